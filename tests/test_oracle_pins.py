@@ -1,0 +1,373 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code (no GPU needed).
+
+Each pin is chosen so that a plausible slip in the oracle -- a wrong nibble or
+bit order, a transposed operand, a dropped bias term, a wrong rounding mode, a
+mis-decoded scale byte -- fails at least one of them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import read_golden, read_golden_rows
+
+DTYPES = ("f32", "f16", "bf16")
+
+
+def _store(vals, dtype):
+    """float values -> storage array (exactly representable values only)."""
+    a = np.asarray(vals, dtype=np.float32)
+    if dtype == "f32":
+        return a
+    t = torch.from_numpy(a).to(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+# --------------------------------------------------------------------------
+# storage formats, against numpy / torch conversions (library routines)
+# --------------------------------------------------------------------------
+
+def test_f16_decode_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.to_f64(bits, "f16")
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_decode_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    got = oracle.to_f64(bits, "bf16")
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def _f32_samples():
+    r = np.random.default_rng(7)
+    rand_bits = r.integers(0, 2**32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    a = [rand_bits.view(np.float32)]
+    # every f16 value and the midpoints between neighbours (ties), nudged both ways
+    h = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    mids = (h[:-1] + h[1:]) / 2
+    for v in (h, mids):
+        v32 = v.astype(np.float32)
+        a += [v32, -v32, np.nextafter(v32, np.float32(np.inf)), np.nextafter(v32, np.float32(0))]
+    # bf16 neighbours and midpoints over a wide exponent range
+    b = np.arange(0, 0x7F80, 7, dtype=np.uint32) << 16
+    bv = b.view(np.float32).astype(np.float64)
+    bm = ((bv[:-1] + bv[1:]) / 2).astype(np.float32)
+    a += [bm, -bm, np.nextafter(bm, np.float32(np.inf))]
+    a += [np.array([65504, 65519.99, 65520, 65536, 1e30, np.inf, -np.inf, 2**-24, 2**-25,
+                    3 * 2**-26, 2**-14, 0.0, -0.0], dtype=np.float32)]
+    out = np.concatenate(a).astype(np.float32)
+    return out[~np.isnan(out)]
+
+
+def test_f32_to_f16_rne_matches_numpy():
+    x = _f32_samples()
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    L = oracle.lib()
+    got = np.array([L.orc_f32_to_f16_rne(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_f32_to_bf16_rne_matches_torch():
+    x = _f32_samples()
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    L = oracle.lib()
+    got = np.array([L.orc_f32_to_bf16_rne(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------------------
+# packing order and the 4-bit worked example
+# --------------------------------------------------------------------------
+
+def _codes(spec):
+    expr, rng_ = spec.split(" for i<")
+    n = int(rng_)
+    return [eval(expr, {"i": i}) for i in range(n)]  # noqa: S307  (fixture text, trusted)
+
+
+@pytest.mark.parametrize("row", read_golden_rows("packing_widths.txt"), ids=lambda r: r[0] + "bit")
+def test_packing_widths_golden(row):
+    bits = int(row[0])
+    codes = _codes(row[1])
+    words = [int(w, 16) for w in row[2].split()]
+    # independent construction: one Python integer as the row's bit stream
+    stream = 0
+    for i, q in enumerate(codes):
+        stream |= q << (bits * i)
+    assert [(stream >> (32 * j)) & 0xFFFFFFFF for j in range(len(words))] == words
+    K = len(codes)
+    q = np.array([codes], dtype=np.uint8)
+    assert oracle.pack(q, bits).reshape(-1).tolist() == words
+    assert oracle.unpack(np.array([words], dtype=np.uint32), bits, K).reshape(-1).tolist() == codes
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 6, 8])
+def test_pack_unpack_roundtrip_random(bits):
+    r = np.random.default_rng(bits)
+    q = r.integers(0, 2**bits, size=(5, 256), dtype=np.int64).astype(np.uint8)
+    p = oracle.pack(q, bits)
+    assert p.shape == (5, 256 * bits // 32)
+    assert np.array_equal(oracle.unpack(p, bits, 256), q)
+    # the stream is dense: every bit of every word belongs to exactly one code
+    ones = oracle.pack(np.full((1, 256), 2**bits - 1, dtype=np.uint8), bits)
+    assert np.all(ones == 0xFFFFFFFF)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_nibble_worked_example(dtype):
+    g = read_golden("nibble_worked_example.txt")
+    words = np.array([[int(w, 0) for w in g["words"].split()]], dtype=np.uint32)
+    assert oracle.unpack(words, 4, 64)[0, :8].tolist() == [int(c) for c in g["codes"].split()]
+    scales = _store([[float(g["scale"])]], dtype)
+    biases = _store([[float(g["bias"])]], dtype)
+    for case in ("a", "b"):
+        xv = np.zeros(64, dtype=np.float32)
+        xv[:8] = [float(v) for v in g[f"case_{case}_x"].split()]
+        out, _ = oracle.qmm(words, scales, biases, _store(xv, dtype), 4, 64, dtype)
+        assert out[0] == float(g[f"case_{case}_out"])
+
+
+# --------------------------------------------------------------------------
+# quantize: invariants and special cases
+# --------------------------------------------------------------------------
+
+def _quant_case(bits, gs, dtype, seed):
+    W = synth.affine_weights(6, 4 * gs, seed)
+    packed, s, b = oracle.quantize(W, bits, gs, dtype)
+    q = oracle.unpack(packed, bits, W.shape[1]).astype(np.int64)
+    sv = oracle.to_f64(s, dtype)
+    bv = oracle.to_f64(b, dtype)
+    return W, q, sv, bv
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("gs", [32, 64, 128])
+@pytest.mark.parametrize("bits", [2, 3, 4, 6, 8])
+def test_quantize_roundtrip_bound(bits, gs, dtype):
+    W, q, sv, bv = _quant_case(bits, gs, dtype, seed=bits * 1000 + gs)
+    L = 2**bits - 1
+    N, K = W.shape
+    w = W.astype(np.float64).reshape(N, K // gs, gs)
+    qg = q.reshape(N, K // gs, gs)
+    s_ = sv[:, :, None]
+    b_ = bv[:, :, None]
+    what = s_ * qg + b_
+    err = np.abs(w - what)
+    mn = w.min(axis=2, keepdims=True)
+    mx = w.max(axis=2, keepdims=True)
+    s32 = ((mx - mn).astype(np.float32) / np.float32(L)).astype(np.float64)
+    slack = s_ * 2.0**-14
+    clamp_bound = np.maximum(s_ / 2, L * np.abs(s32 - s_) + np.abs(mn - b_))
+    clamped = (qg == 0) | (qg == L)
+    strict = np.broadcast_to(s_ / 2 + slack, err.shape)
+    assert np.all(err[~clamped] <= strict[~clamped])
+    assert np.all(err <= np.broadcast_to(clamp_bound + slack, err.shape))
+    assert q.min() >= 0 and q.max() <= L
+    # the group minimum and maximum are reproduced within s'/2 (plus rounding of s', b')
+    assert np.all(np.abs(mn - (b_ + s_ * qg.min(axis=2, keepdims=True))) <= clamp_bound + slack)
+    if dtype == "f32":
+        # no rounding of s and b: the strict bound holds everywhere
+        assert np.all(err <= s_ / 2 + slack)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("bits", [2, 3, 4, 6, 8])
+def test_quantize_codes_are_nearest(bits, dtype):
+    """Brute force: no other code is closer to w than the chosen one."""
+    W, q, sv, bv = _quant_case(bits, 32, dtype, seed=5 + bits)
+    N, K = W.shape
+    L = 2**bits - 1
+    codes = np.arange(L + 1, dtype=np.float64)
+    s_ = np.repeat(sv, 32, axis=1)
+    b_ = np.repeat(bv, 32, axis=1)
+    w = W.astype(np.float64)
+    dist_all = np.abs(w[:, :, None] - (s_[:, :, None] * codes + b_[:, :, None]))
+    chosen = np.take_along_axis(dist_all, q[:, :, None], axis=2)[:, :, 0]
+    assert np.all(chosen <= dist_all.min(axis=2) + s_ * 2.0**-14)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_quantize_constant_group_and_ramp(bits, dtype):
+    L = 2**bits - 1
+    gs = 64
+    # ramp w_i = b' + c_i * s' with codes c_i spanning 0..L and s', b' exact in every dtype
+    s_exact, b_exact = 2.0**-6, -0.25
+    i = np.arange(gs)
+    codes = (i * L) // (gs - 1)
+    ramp = (b_exact + codes * s_exact).astype(np.float32)
+    const = np.full(gs, 0.0123, dtype=np.float32)
+    W = np.stack([ramp, const]).astype(np.float32)
+    packed, s, b = oracle.quantize(W, bits, gs, dtype)
+    q = oracle.unpack(packed, bits, gs)
+    sv = oracle.to_f64(s, dtype)
+    bv = oracle.to_f64(b, dtype)
+    assert sv[0, 0] == s_exact and bv[0, 0] == b_exact
+    assert q[0].tolist() == codes.tolist()
+    assert sv[1, 0] == 0.0 and np.all(q[1] == 0)
+    assert bv[1, 0] == oracle.to_f64(_store([0.0123], dtype), dtype)[0]
+    what = oracle.dequantize(packed, s, b, bits, gs, dtype, gs)
+    assert np.all(what[1] == bv[1, 0])
+
+
+# --------------------------------------------------------------------------
+# qmm / qmv: the dot product against a library matmul
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("bits,gs", [(4, 64), (3, 32), (6, 128), (2, 64), (8, 32)])
+def test_qmm_matches_library_matmul(bits, gs, dtype):
+    N, K, M = 9, 3 * gs, 5
+    W = synth.affine_weights(N, K, seed=11)
+    packed, s, b = oracle.quantize(W, bits, gs, dtype)
+    x = synth.activations(M, K, dtype, seed=12)
+    out, absdot = oracle.qmm(packed, s, b, x, bits, gs, dtype)
+    what = oracle.dequantize(packed, s, b, bits, gs, dtype, K)
+    xf = oracle.to_f64(x, dtype)
+    ref = torch.from_numpy(xf) @ torch.from_numpy(what).T          # [M, N] float64
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(absdot, (torch.from_numpy(xf).abs() @ torch.from_numpy(what).abs().T).numpy(),
+                               rtol=1e-12, atol=1e-12)
+    # the bias-hoisted form of the pages (scale * sum q*x + bias * sum x) gives the same value
+    q = oracle.unpack(packed, bits, K).astype(np.float64).reshape(N, K // gs, gs)
+    sv = oracle.to_f64(s, dtype)
+    bv = oracle.to_f64(b, dtype)
+    xg = xf.reshape(M, K // gs, gs)
+    hoisted = np.einsum("ng,mng->mn", sv, np.einsum("ngi,mgi->mng", q, xg)) + \
+        np.einsum("ng,mg->mn", bv, xg.sum(axis=2))
+    np.testing.assert_allclose(out, hoisted, rtol=1e-11, atol=1e-12)
+
+
+def test_qmm_rows_and_sampling_consistent():
+    N, K, M, gs = 17, 256, 3, 64
+    W = synth.affine_weights(N, K, seed=3)
+    packed, s, b = oracle.quantize(W, 4, gs, "bf16")
+    x = synth.activations(M, K, "bf16", seed=4)
+    full, _ = oracle.qmm(packed, s, b, x, 4, gs, "bf16")
+    rows = np.array([16, 0, 5], dtype=np.int64)
+    part, _ = oracle.qmm(packed, s, b, x, 4, gs, "bf16", rows=rows)
+    assert np.array_equal(part, full[:, rows])
+    for m in range(M):
+        one, _ = oracle.qmm(packed, s, b, x[m], 4, gs, "bf16")
+        assert np.array_equal(one, full[m])
+
+
+# --------------------------------------------------------------------------
+# Q8_0
+# --------------------------------------------------------------------------
+
+def test_q8_0_worked_example():
+    g = read_golden("q8_0_worked_example.txt")
+    words = np.array([int(w, 0) for w in g["words"].split()], dtype=np.uint32)
+    w = oracle.q8_0_dequant_block(words)
+    assert w.tolist() == [0.5 * (j - 16) for j in range(32)]
+    blocks = words.reshape(1, 1, 9)
+    a, _ = oracle.q8_0_gemv(blocks, np.ones(32, dtype=np.float32))
+    b, _ = oracle.q8_0_gemv(blocks, np.arange(32, dtype=np.float32))
+    assert a[0] == float(g["case_a_out"]) and b[0] == float(g["case_b_out"])
+
+
+def test_q8_0_closed_forms():
+    N, K = 7, 32 * 12
+    blocks = synth.q8_0_blocks(N, K, seed=9)
+    d = oracle.to_f64((blocks[:, :, 0] & 0xFFFF).astype(np.uint16), "f16")
+    ones = blocks.copy()
+    ones[:, :, 1:] = 0x01010101                       # q == 1 everywhere
+    out, _ = oracle.q8_0_gemv(ones, np.ones(K, dtype=np.float32))
+    np.testing.assert_allclose(out, 32 * d.sum(axis=1), rtol=1e-14)
+    ramp = blocks.copy()
+    qb = (np.arange(32) - 16).astype(np.int8).view(np.uint8).view("<u4")
+    ramp[:, :, 1:] = qb                               # q_j = j - 16
+    out, _ = oracle.q8_0_gemv(ramp, np.ones(K, dtype=np.float32))
+    np.testing.assert_allclose(out, -16 * d.sum(axis=1), rtol=1e-14)
+    # the high half of word 0 is not part of the scale
+    junk = blocks.copy()
+    junk[:, :, 0] |= 0xABCD0000
+    x = synth.f32_vector(K, seed=1)
+    assert np.array_equal(oracle.q8_0_gemv(junk, x)[0], oracle.q8_0_gemv(blocks, x)[0])
+    # the result is sum over blocks of d * (q . x): compare with a library matmul
+    q = blocks[:, :, 1:].copy().view(np.uint8).view(np.int8).reshape(N, K).astype(np.float64)
+    ref = (q * np.repeat(d, 32, axis=1)) @ x.astype(np.float64)
+    np.testing.assert_allclose(oracle.q8_0_gemv(blocks, x)[0], ref, rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Q4_K
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("row", read_golden_rows("q4k_scale_min.txt"), ids=lambda r: r[0])
+def test_q4k_scale_min_table(row):
+    sc12 = np.array([int(b, 16) for b in row[1].split()], dtype=np.uint8)
+    want = [tuple(int(v) for v in p.split(",")) for p in row[2].split()]
+    assert [oracle.q4_k_scale_min(sc12, j) for j in range(8)] == want
+
+
+def _encode_scale_min(sc, m):
+    """Pack eight 6-bit (scale, min) pairs into 12 bytes following the byte
+    placement the decode implies (written from the layout, not from the
+    decode): bytes 0-3 low 6 bits = sc0..3, bytes 4-7 low 6 bits = m0..3,
+    bytes 8-11 = sc4..7 low nibble | m4..7 low nibble << 4, and the top two
+    bits of bytes 0-3 / 4-7 carry bits 4-5 of sc4..7 / m4..7."""
+    b = [0] * 12
+    for j in range(4):
+        b[j] = sc[j] | ((sc[j + 4] >> 4) << 6)
+        b[j + 4] = m[j] | ((m[j + 4] >> 4) << 6)
+        b[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    return np.array(b, dtype=np.uint8)
+
+
+def test_q4k_scale_min_bijection():
+    r = np.random.default_rng(21)
+    for _ in range(3000):
+        sc = r.integers(0, 64, size=8).tolist()
+        m = r.integers(0, 64, size=8).tolist()
+        got = [oracle.q4_k_scale_min(_encode_scale_min(sc, m), j) for j in range(8)]
+        assert got == list(zip(sc, m))
+
+
+def test_q4k_element_order():
+    g = read_golden("q4k_element_order.txt")
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0:2] = np.array([int(g["d_bits"], 0)], dtype="<u2").view(np.uint8)
+    blk[2:4] = np.array([int(g["dmin_bits"], 0)], dtype="<u2").view(np.uint8)
+    blk[4:16] = [int(b, 16) for b in g["scales"].split()]
+    blk[16:] = np.arange(128, dtype=np.uint8)
+    w = oracle.q4_k_dequant_block(blk)
+    for item in g["expect"].split():
+        e, v = item.split(":")
+        assert w[int(e)] == float(v), e
+
+
+def test_q4k_gemv_matches_library_matmul():
+    N, K = 5, 512
+    blocks = synth.q4_k_blocks(N, K, seed=2)
+    x = synth.f32_vector(K, seed=3)
+    what = np.stack([np.concatenate([oracle.q4_k_dequant_block(blocks[n, b]) for b in range(K // 256)])
+                     for n in range(N)])
+    out, absdot = oracle.q4_k_gemv(blocks, x)
+    np.testing.assert_allclose(out, what @ x.astype(np.float64), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(absdot, np.abs(what) @ np.abs(x.astype(np.float64)), rtol=1e-12)
+    rows = np.array([4, 1], dtype=np.int64)
+    assert np.array_equal(oracle.q4_k_gemv(blocks, x, rows=rows)[0], out[rows])
+
+
+def test_oracle_rejects_bad_shapes():
+    W = np.zeros((2, 96), dtype=np.float32)
+    with pytest.raises(ValueError):
+        oracle.quantize(W, 4, 64, "bf16")          # K not a multiple of the group size
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((2, 64), np.float32), 5, 64, "bf16")   # unsupported width
+    with pytest.raises(ValueError):
+        oracle.q4_k_gemv(np.zeros((1, 1, 144), np.uint8), np.zeros(100, np.float32))
