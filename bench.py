@@ -1,0 +1,538 @@
+"""Throughput benchmark of the GB300 affine group-quantized GEMV / small-M GEMM
+library (libgai4.so).
+
+One "step" is one pass over the whole hot path on seeded synthetic inputs
+resident in HBM:
+  * qmv, 4-bit, group size 64, bf16: (N, K) = 4096x4096, 5120x5120,
+    14336x5120, 5120x14336, 27648x5120
+  * qmm_t, 4-bit, group size 64, bf16, split-K: (K x N, M) = 2048x2048/22,
+    4096x4096/16, 10752x2048/85, 14336x4096/33, 17408x5120/56, 5120x17408/28,
+    256x4096/40, and 4096x4096/8
+  * Q8_0 and Q4_K GEMV (f32 activations): 4096x4096 and 14336x5120
+The metric is effective GB/s = algorithmic bytes (packed weights + scales +
+biases + activations + outputs; blocks + activations + outputs for Q8_0/Q4_K)
+per unit time. Each kernel family of the step is one CUDA graph, bracketed by
+CUDA events on the launching stream; the step's weights (~0.5 GB) exceed the
+129 MB L2 many times, so every call streams its weights from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU
+("replicas only": the path has no exchange step); rank 0 prints one JSON line.
+`--impl reference` times the CPU oracle on a bounded sample of the same work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "qmv/qmm_t effective HBM GB/s (% of GB300 peak), 4-bit gs64 bf16, M=1..85"
+UNIT = "GB/s"
+
+QMV_SHAPES = [(4096, 4096), (5120, 5120), (14336, 5120), (5120, 14336), (27648, 5120)]   # (N, K)
+QMM_SHAPES = [(2048, 2048, 22), (4096, 4096, 16), (10752, 2048, 85), (14336, 4096, 33),  # (K, N, M)
+              (17408, 5120, 56), (5120, 17408, 28), (256, 4096, 40), (4096, 4096, 8)]
+BLOCKQ_SHAPES = [(4096, 4096), (14336, 5120)]                                              # (N, K)
+BITS, GS = 4, 64
+
+KERNEL_SOURCES = {
+    "qmv": ["gemm_affine_int4_gb300/csrc/affine_gemv.cuh", "gemm_affine_int4_gb300/csrc/common.cuh"],
+}
+
+
+def affine_bytes(M, N, K, tbytes=2):
+    return N * K * BITS // 8 + 2 * N * (K // GS) * tbytes + M * K * tbytes + M * N * tbytes
+
+
+def q8_bytes(N, K):
+    return N * (K // 32) * 36 + K * 4 + N * 4
+
+
+def q4k_bytes(N, K):
+    return N * (K // 256) * 144 + K * 4 + N * 4
+
+
+def step_bytes():
+    fam = {
+        "qmv": sum(affine_bytes(1, N, K) for N, K in QMV_SHAPES),
+        "qmm_t": sum(affine_bytes(M, N, K) for K, N, M in QMM_SHAPES),
+        "q8_0": sum(q8_bytes(N, K) for N, K in BLOCKQ_SHAPES),
+        "q4_k": sum(q4k_bytes(N, K) for N, K in BLOCKQ_SHAPES),
+    }
+    return fam
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(family):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if the summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{family}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != source_hash(KERNEL_SOURCES[family]):
+        return None
+    try:
+        return float(vals["dram_bytes_per_step"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def build_workload(torch, g4, dev, seed=0):
+    """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
+    GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
+    blocks from the shared seeded generators."""
+    import synth
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    bf = torch.bfloat16
+    calls = {"qmv": [], "qmm_t": [], "q8_0": [], "q4_k": []}
+
+    def qweights(N, K):
+        w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * 0.02
+        p, s, b = g4.gai4_quantize(w, BITS, GS, bf)
+        del w
+        return p, s, b
+
+    for N, K in QMV_SHAPES:
+        p, s, b = qweights(N, K)
+        x = torch.randn((K,), generator=gen, device=dev).to(bf)
+        out = torch.empty((N,), dtype=bf, device=dev)
+        calls["qmv"].append(dict(kind="qmv", p=p, s=s, b=b, x=x, out=out, M=1, N=N, K=K,
+                                 bytes=affine_bytes(1, N, K)))
+    for K, N, M in QMM_SHAPES:
+        p, s, b = qweights(N, K)
+        x = torch.randn((M, K), generator=gen, device=dev).to(bf)
+        out = torch.empty((M, N), dtype=bf, device=dev)
+        ws = g4.gai4_qmm_t_workspace_bytes(M, N, K, BITS, GS, bf, 0)
+        wsp = torch.empty(max(ws, 16) // 4 + 4, dtype=torch.float32, device=dev)
+        calls["qmm_t"].append(dict(kind="qmm_t", p=p, s=s, b=b, x=x, out=out, ws=wsp, M=M, N=N, K=K,
+                                   bytes=affine_bytes(M, N, K)))
+    for i, (N, K) in enumerate(BLOCKQ_SHAPES):
+        blk8 = torch.from_numpy(synth.q8_0_blocks(N, K, 300 + i).view(np.int32)).to(dev)
+        blk4 = torch.from_numpy(synth.q4_k_blocks(N, K, 302 + i)).to(dev)
+        x8 = torch.from_numpy(synth.f32_vector(K, 301 + i)).to(dev)
+        x4 = torch.from_numpy(synth.f32_vector(K, 303 + i)).to(dev)
+        calls["q8_0"].append(dict(kind="q8_0", blocks=blk8, x=x8, out=torch.empty(N, device=dev), N=N, K=K,
+                                  bytes=q8_bytes(N, K)))
+        calls["q4_k"].append(dict(kind="q4_k", blocks=blk4, x=x4, out=torch.empty(N, device=dev), N=N, K=K,
+                                  bytes=q4k_bytes(N, K)))
+    torch.cuda.synchronize()
+    return calls
+
+
+def issue(g4, c):
+    k = c["kind"]
+    if k == "qmv":
+        g4.gai4_qmv(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS)
+    elif k == "qmm_t":
+        g4.gai4_qmm_t(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
+                      workspace=c["ws"])
+    elif k == "q8_0":
+        g4.gai4_q8_0_gemv(c["blocks"], c["x"], out=c["out"])
+    else:
+        g4.gai4_q4_k_gemv(c["blocks"], c["x"], out=c["out"])
+
+
+def kernel_launches_per_step(g4, calls, torch):
+    n = 0
+    for fam, cs in calls.items():
+        for c in cs:
+            if fam == "qmm_t":
+                path, splits = g4.gai4_qmm_t_plan(c["M"], c["N"], c["K"], BITS, GS, torch.bfloat16, 0,
+                                                  c["ws"].numel() * 4)
+                n += 2 if splits > 1 else 1
+            else:
+                n += 1
+    return n
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import gemm_affine_int4_gb300 as g4
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    g4.lib()
+    calls = build_workload(torch, g4, dev)
+    fam_bytes = {f: sum(c["bytes"] for c in cs) for f, cs in calls.items()}
+    total_bytes = sum(fam_bytes.values())
+    stream = torch.cuda.Stream(device=dev)
+
+    # eager warm-up (lazy library set-up happens outside any capture)
+    with torch.cuda.stream(stream):
+        for cs in calls.values():
+            for c in cs:
+                issue(g4, c)
+    stream.synchronize()
+    st = g4.gai4_last_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # one CUDA graph per kernel family
+    graphs = {}
+    for fam, cs in calls.items():
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for c in cs:
+                issue(g4, c)
+        graphs[fam] = gr
+    fams = list(calls)
+
+    def one_step(evs=None):
+        for i, fam in enumerate(fams):
+            if evs is not None:
+                evs[i][0].record(stream)
+            graphs[fam].replay()
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fams]
+          for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        reps = max(1, args.inner)
+        for k in range(K):
+            for _ in range(reps - 1):
+                one_step()
+            one_step(ev[k])
+        t1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    steps_total = K * reps
+    fam_ms = {fam: sum(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)) / K for i, fam in enumerate(fams)}
+    st = g4.gai4_last_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    # end to end through the public API: per step, H2D of every call's
+    # activations from pinned host memory, the calls, D2H of every output
+    e2e = run_e2e(torch, g4, calls, stream, args)
+
+    ms_per_step = elapsed_ms / steps_total
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * total_bytes / (ms_per_step * 1e-3) / 1e9
+
+    hbm, tflops, peak_src = load_peaks()
+    dom = max(fam_ms, key=fam_ms.get)
+    dom_ms = fam_ms[dom]
+    n_launch = len(calls[dom])
+    achieved = fam_bytes[dom] / (dom_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(dom)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 activations, 4-bit weights, fp32 accumulate (f32 activations for Q8_0/Q4_K)",
+        "data": "synthetic (seeded; W~N(0,0.02) quantized on the GPU, x~N(0,1))",
+        "config": {
+            "workload": "one pass of the hot path: qmv 4-bit gs64 bf16 x5 shapes (4096^2..27648x5120); "
+                        "qmm_t 4-bit gs64 bf16 split-K (KxN,M) 2048x2048/22, 4096x4096/16, 10752x2048/85, "
+                        "14336x4096/33, 17408x5120/56, 5120x17408/28, 256x4096/40, 4096x4096/8; "
+                        "Q8_0 and Q4_K GEMV 4096x4096 and 14336x5120 (f32 x)",
+            "bytes_per_step": total_bytes, "calls_per_step": sum(len(v) for v in calls.values()),
+            "l2": "no flush: %.0f MB of distinct weights per step > 129 MB L2" % (total_bytes / 1e6),
+            "timing": "each kernel family one CUDA graph; CUDA events on the launching stream",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "breakdown": {fam: {"ms": round(fam_ms[fam], 5), "GB/s": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9 / hbm, 3),
+                            "bytes": fam_bytes[fam]} for fam in fams},
+        "roofline": {"kernel": {"qmv": "affine_gemv_kernel (qmv, M=1)", "qmm_t": "qmm_t family",
+                                "q8_0": "q8_0_gemv_kernel", "q4_k": "q4_k_gemv_kernel"}[dom],
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
+                     "launches_per_step": n_launch,
+                     "algorithmic_bytes_per_launch": round(fam_bytes[dom] / n_launch),
+                     "avg_launch_us": round(dom_ms * 1e3 / n_launch, 3),
+                     "traffic": None if traffic is None else round(traffic / n_launch)},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return res
+
+
+def run_e2e(torch, g4, calls, stream, args):
+    """Same workload through the public calls with host buffers: pinned host
+    activations copied in and every output copied back inside the timed region
+    (captured in one CUDA graph with the calls, replayed per step)."""
+    host_in, host_out = [], []
+    order = [c for cs in calls.values() for c in cs]
+    for c in order:
+        host_in.append(c["x"].detach().cpu().pin_memory())
+        host_out.append(torch.empty(c["out"].shape, dtype=c["out"].dtype, pin_memory=True))
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for c, hi, ho in zip(order, host_in, host_out):
+            c["x"].copy_(hi, non_blocking=True)
+            issue(g4, c)
+            ho.copy_(c["out"], non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            gr.replay()
+    stream.synchronize()
+    K = max(args.steps, 1)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(K):
+            gr.replay()
+        t1.record(stream)
+    stream.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    total = sum(c["bytes"] for c in order)
+    return {"value": round(total / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_work(fraction):
+    """The oracle on a sample of the step: every call of the step, restricted
+    to a deterministic subset of its output rows (all x rows)."""
+    import oracle
+    import synth
+    items = []
+    for i, (N, K) in enumerate(QMV_SHAPES):
+        items.append(("affine", 1, N, K, i))
+    for i, (K, N, M) in enumerate(QMM_SHAPES):
+        items.append(("affine", M, N, K, 100 + i))
+    for i, (N, K) in enumerate(BLOCKQ_SHAPES):
+        items.append(("q8_0", 1, N, K, 300 + i))
+        items.append(("q4_k", 1, N, K, 302 + i))
+    prepared = []
+    for kind, M, N, K, seed in items:
+        nr = max(8, int(round(N * fraction)))
+        rows = np.linspace(0, N - 1, nr).astype(np.int64)
+        if kind == "affine":
+            W = synth.affine_weights(nr, K, seed)      # the sampled rows' weights
+            packed, s, b = oracle.quantize(W, BITS, GS, "bf16")
+            x = synth.activations(M, K, "bf16", seed + 1)
+            byt = affine_bytes(M, N, K) * nr / N
+            prepared.append((lambda p=packed, s_=s, b_=b, x_=x: oracle.qmm(p, s_, b_, x_, BITS, GS, "bf16"), byt))
+        elif kind == "q8_0":
+            blk = synth.q8_0_blocks(nr, K, seed)
+            x = synth.f32_vector(K, seed + 1)
+            prepared.append((lambda b_=blk, x_=x: oracle.q8_0_gemv(b_, x_), q8_bytes(N, K) * nr / N))
+        else:
+            blk = synth.q4_k_blocks(nr, K, seed)
+            x = synth.f32_vector(K, seed + 1)
+            prepared.append((lambda b_=blk, x_=x: oracle.q4_k_gemv(b_, x_), q4k_bytes(N, K) * nr / N))
+    return prepared
+
+
+def cpu_baseline(target_s=12.0):
+    """Time the oracle (single thread, binary64) on a bounded sample."""
+    frac = 1.0 / 512
+    work = _oracle_work(frac)
+    t = time.perf_counter()
+    for fn, _ in work:
+        fn()
+    dt = time.perf_counter() - t
+    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
+    work = _oracle_work(frac)
+    byt = sum(b for _, b in work)
+    t = time.perf_counter()
+    for fn, _ in work:
+        fn()
+    dt = time.perf_counter() - t
+    return {"value": round(byt / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"every call of the step on {frac:.4%} of its output rows (all x rows), "
+                      f"binary64 C oracle, single thread, {dt:.1f} s"}
+
+
+def run_reference(args):
+    steps = []
+    frac = None
+    byt_total = 0.0
+    t_total = 0.0
+    target = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    frac = 1.0 / 512
+    work = _oracle_work(frac)
+    t = time.perf_counter()
+    for fn, _ in work:
+        fn()
+    dt = time.perf_counter() - t
+    frac = min(1.0, frac * max(1.0, target / max(dt, 1e-3)))
+    work = _oracle_work(frac)
+    byt = sum(b for _, b in work)
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        for fn, _ in work:
+            fn()
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            steps.append(dt)
+            byt_total += byt
+            t_total += dt
+    value = byt_total / t_total / 1e9
+    ms = 1e3 * t_total / max(1, len(steps))
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+            "config": {"workload": "the same step as the GPU arm, each call restricted to "
+                                   f"{frac:.4%} of its output rows"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{frac:.4%} of output rows of every call, single thread"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--inner", type=int, default=1, help="untimed-event steps per timed step")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

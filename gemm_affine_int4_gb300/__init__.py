@@ -1,0 +1,212 @@
+"""Python binding of libgai4.so, the GB300 (sm_103a) affine group-quantized
+GEMV / small-M GEMM library. Argument marshalling only: every function here
+calls the C entry point of the same name (include/gai4.h) with device pointers
+of PyTorch tensors and the current CUDA stream; all arithmetic runs in the
+library's CUDA kernels. There is no fallback: if libgai4.so is not built, or a
+tensor is not on a CUDA device, the call raises.
+
+Tensor conventions (row-major, contiguous, on one CUDA device):
+  w_packed  int32/uint32 [N, K*bits/32]      scales, biases  T [N, K/group_size]
+  x         T [K] (qmv) or [M, K] (qmm_t)    out             T [N] or [M, N]
+with T = torch.bfloat16, torch.float16 or torch.float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgai4.so")
+
+GAI4_OK = 0
+GAI4_ERR_INVALID_ARG = 1
+GAI4_ERR_UNSUPPORTED = 2
+GAI4_ERR_MISALIGNED = 3
+GAI4_ERR_WORKSPACE = 4
+GAI4_ERR_CUDA = 5
+GAI4_ERR_TIMEOUT = 6
+
+_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+# name -> (argtypes, restype) of every exported entry point
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+SIGNATURES = {
+    "gai4_version": ([], _I),
+    "gai4_status_string": ([_I], ctypes.c_char_p),
+    "gai4_quantize": ([_P, _P, _P, _P, _I, _I, _I, _I64, _I64, _P], _I),
+    "gai4_unpack": ([_P, _P, _I, _I64, _I64, _P], _I),
+    "gai4_dequantize": ([_P, _P, _P, _P, _I, _I, _I, _I64, _I64, _P], _I),
+    "gai4_qmv": ([_P, _P, _P, _P, _P, _I, _I, _I, _I64, _I64, _P], _I),
+    "gai4_qmm_t": ([_P, _P, _P, _P, _P, _I, _I, _I, _I64, _I64, _I64, _I, _P, ctypes.c_size_t, _P], _I),
+    "gai4_qmm_t_workspace_bytes": ([_I64, _I64, _I64, _I, _I, _I, _I], ctypes.c_size_t),
+    "gai4_qmm_t_plan": ([_I64, _I64, _I64, _I, _I, _I, _I, ctypes.c_size_t, ctypes.POINTER(_I),
+                         ctypes.POINTER(_I)], _I),
+    "gai4_q8_0_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
+    "gai4_q4_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
+    "gai4_last_device_status": ([_P], _I),
+}
+
+
+class Gai4Error(RuntimeError):
+    def __init__(self, name: str, status: int):
+        self.status = status
+        super().__init__(f"{name}: {gai4_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgai4.so (built in-tree by __graft_entry__.build() or
+    `python -m gemm_affine_int4_gb300.build`)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m gemm_affine_int4_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (argtypes, restype) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = argtypes
+            fn.restype = restype
+        _lib = L
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("gai4: tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("gai4: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name: str, st: int):
+    if st != GAI4_OK:
+        raise Gai4Error(name, st)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE:
+        raise ValueError(f"gai4: unsupported dtype {t.dtype}")
+    return _DTYPE[t.dtype]
+
+
+def gai4_version() -> int:
+    return lib().gai4_version()
+
+
+def gai4_status_string(status: int) -> str:
+    return lib().gai4_status_string(int(status)).decode()
+
+
+def gai4_quantize(w: torch.Tensor, bits: int = 4, group_size: int = 64, dtype=torch.bfloat16,
+                  w_packed=None, scales=None, biases=None, stream=None):
+    """Affine group quantize w [N, K] float32 -> (w_packed, scales, biases)."""
+    N, K = w.shape
+    if w_packed is None:
+        w_packed = torch.empty((N, K * bits // 32), dtype=torch.int32, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // group_size), dtype=dtype, device=w.device)
+    if biases is None:
+        biases = torch.empty((N, K // group_size), dtype=dtype, device=w.device)
+    _check("gai4_quantize", lib().gai4_quantize(_ptr(w), _ptr(w_packed), _ptr(scales), _ptr(biases),
+                                                _dtype(scales), bits, group_size, N, K, _stream(stream)))
+    return w_packed, scales, biases
+
+
+def gai4_unpack(w_packed: torch.Tensor, bits: int, K: int, q_out=None, stream=None) -> torch.Tensor:
+    N = w_packed.shape[0]
+    if q_out is None:
+        q_out = torch.empty((N, K), dtype=torch.uint8, device=w_packed.device)
+    _check("gai4_unpack", lib().gai4_unpack(_ptr(w_packed), _ptr(q_out), bits, N, K, _stream(stream)))
+    return q_out
+
+
+def gai4_dequantize(w_packed, scales, biases, bits: int = 4, group_size: int = 64, out=None, stream=None):
+    N = w_packed.shape[0]
+    K = w_packed.shape[1] * 32 // bits
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=w_packed.device)
+    _check("gai4_dequantize", lib().gai4_dequantize(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(out),
+                                                    _dtype(scales), bits, group_size, N, K, _stream(stream)))
+    return out
+
+
+def gai4_qmv(w_packed, scales, biases, x, out=None, bits: int = 4, group_size: int = 64, stream=None):
+    """out[n] = sum_k (s q + b)[n, k] x[k]."""
+    N = w_packed.shape[0]
+    K = x.shape[-1]
+    if out is None:
+        out = torch.empty((N,), dtype=x.dtype, device=x.device)
+    _check("gai4_qmv", lib().gai4_qmv(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x), _ptr(out),
+                                      _dtype(x), bits, group_size, N, K, _stream(stream)))
+    return out
+
+
+def gai4_qmm_t_workspace_bytes(M: int, N: int, K: int, bits: int, group_size: int, dtype, split_k: int = 0) -> int:
+    return int(lib().gai4_qmm_t_workspace_bytes(M, N, K, bits, group_size, _DTYPE[dtype], split_k))
+
+
+def gai4_qmm_t_plan(M: int, N: int, K: int, bits: int, group_size: int, dtype, split_k: int = 0,
+                    workspace_bytes: int = 0):
+    """(path, splits): path 0 = CUDA-core kernel, 1 = tensor core."""
+    path = ctypes.c_int()
+    splits = ctypes.c_int()
+    _check("gai4_qmm_t_plan", lib().gai4_qmm_t_plan(M, N, K, bits, group_size, _DTYPE[dtype], split_k,
+                                                    workspace_bytes, ctypes.byref(path), ctypes.byref(splits)))
+    return path.value, splits.value
+
+
+def gai4_qmm_t(w_packed, scales, biases, x, out=None, bits: int = 4, group_size: int = 64, split_k: int = 0,
+               workspace=None, stream=None):
+    """out[m, n] = sum_k x[m, k] (s q + b)[n, k]. `workspace` (any dtype,
+    device) holds the fp32 split-K partials; without one no split is used
+    unless split_k forces it, in which case one is allocated here."""
+    M, K = x.shape
+    N = w_packed.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if workspace is None and split_k > 1:
+        nbytes = gai4_qmm_t_workspace_bytes(M, N, K, bits, group_size, x.dtype, split_k)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("gai4_qmm_t", lib().gai4_qmm_t(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x), _ptr(out),
+                                          _dtype(x), bits, group_size, M, N, K, split_k, _ptr(workspace),
+                                          ws_bytes, _stream(stream)))
+    return out
+
+
+def gai4_q8_0_gemv(blocks, x, out=None, stream=None):
+    """blocks [N, K/32, 9] int32/uint32, x [K] float32 -> out [N] float32."""
+    N = blocks.shape[0]
+    K = x.shape[-1]
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float32, device=x.device)
+    _check("gai4_q8_0_gemv", lib().gai4_q8_0_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
+    return out
+
+
+def gai4_q4_k_gemv(blocks, x, out=None, stream=None):
+    """blocks [N, K/256, 144] uint8, x [K] float32 -> out [N] float32."""
+    N = blocks.shape[0]
+    K = x.shape[-1]
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float32, device=x.device)
+    _check("gai4_q4_k_gemv", lib().gai4_q4_k_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
+    return out
+
+
+def gai4_last_device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device status word."""
+    return int(lib().gai4_last_device_status(_stream(stream)))

@@ -1,0 +1,274 @@
+// api.cu -- the C ABI of libgai4.so (declared in include/gai4.h): argument
+// validation, planning (kernel choice, K split) and launch. No allocation.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gai4 {
+
+// Device status word: kernels with bounded waits record GAI4_ERR_TIMEOUT here.
+__device__ int g_device_status;
+
+static int* status_ptr() {
+    static int* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool valid_bits(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 6 || bits == 8; }
+static bool valid_gs(int gs) { return gs == 32 || gs == 64 || gs == 128; }
+static bool valid_dtype(int d) { return d == GAI4_F32 || d == GAI4_F16 || d == GAI4_BF16; }
+
+// common checks of the affine entry points (shape part)
+static gai4_status check_affine_shape(int dtype, int bits, int gs, int64_t N, int64_t K) {
+    if (!valid_dtype(dtype) || !valid_bits(bits) || !valid_gs(gs)) return GAI4_ERR_UNSUPPORTED;
+    if (N <= 0 || K <= 0 || K % gs != 0 || (K * bits) % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    return GAI4_OK;
+}
+
+static gai4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GAI4_OK : GAI4_ERR_CUDA; }
+
+// CUDA-core affine kernel: choose x rows per CTA, rows per warp and K split
+static AffineGemvLaunch plan_affine(const uint32_t* w, const void* sc, const void* bi, const void* x, void* out,
+                                    int bits, int gs, int64_t M, int64_t N, int64_t K) {
+    AffineGemvLaunch L;
+    L.w = w;
+    L.scales = sc;
+    L.biases = bi;
+    L.x = x;
+    L.out = out;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.bits = bits;
+    L.group_size = gs;
+    L.mb = M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8));
+    L.rows_per_warp = L.mb == 1 ? 4 : (L.mb == 8 ? 1 : 2);
+    const int E = (bits == 6 || bits == 8) ? 16 : 32;
+    const int64_t its_total = (K / E + 31) / 32;   // warp iterations per row
+    const int64_t mblocks = (M + L.mb - 1) / L.mb;
+    const int64_t target = 4LL * num_sms();
+    int S = 1;
+    while (S < 8 && 2 * S <= its_total) {
+        const int64_t rows_per_cta = (8 / S) * L.rows_per_warp;
+        if (((N + rows_per_cta - 1) / rows_per_cta) * mblocks >= target) break;
+        S *= 2;
+    }
+    L.ksplit = S;
+    return L;
+}
+
+static cudaError_t launch_affine(const AffineGemvLaunch& L, int dtype, cudaStream_t s) {
+    switch (dtype) {
+    case GAI4_F32: return launch_affine_gemv_f32(L, s);
+    case GAI4_F16: return launch_affine_gemv_f16(L, s);
+    default: return launch_affine_gemv_bf16(L, s);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// qmm_t planning: path (CUDA-core / tensor core) and K split
+// ---------------------------------------------------------------------------
+static const int64_t kTcMinM = 9;   // tensor-core path from this many x rows up (bf16/f16)
+
+// a split S is legal when every K range is a multiple of 64 and of the group
+// size, and at least 256 long; K < 512 is never split (MLX PR, split-K route)
+static bool split_legal(int64_t K, int gs, int S) {
+    if (S == 1) return true;
+    if (S < 1 || S > 4 || K < 512) return false;
+    const int64_t unit = gs > 64 ? gs : 64;
+    if (K % (S * unit) != 0) return false;
+    return K / S >= 256;
+}
+
+static int auto_split(int64_t M, int64_t N, int64_t K, int gs, size_t ws_bytes, bool tc) {
+    if (!tc) return 1;
+    const int64_t tiles = (N + 127) / 128;
+    const int64_t sms = num_sms();
+    int best = 1;
+    for (int S = 2; S <= 4; ++S) {
+        if (!split_legal(K, gs, S)) continue;
+        if ((size_t)S * (size_t)M * (size_t)N * 4u > ws_bytes) continue;
+        if (tiles * best >= sms) break;   // already fills the GPU
+        best = S;
+    }
+    return best;
+}
+
+static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, int dtype, int split_k,
+                            size_t ws_bytes, bool unlimited_ws, int* path, int* splits) {
+    gai4_status st = check_affine_shape(dtype, bits, gs, N, K);
+    if (st != GAI4_OK) return st;
+    if (M <= 0) return GAI4_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > 4) return GAI4_ERR_UNSUPPORTED;
+    const bool tc = dtype != GAI4_F32 && M >= kTcMinM && qmm_tc_supported(M, N, K, bits, gs);
+    int S;
+    if (split_k == 0) {
+        S = auto_split(M, N, K, gs, unlimited_ws ? (size_t)-1 : ws_bytes, tc);
+    } else {
+        if (!split_legal(K, gs, split_k)) return GAI4_ERR_UNSUPPORTED;
+        if (split_k > 1 && !tc) return GAI4_ERR_UNSUPPORTED;   // only the tensor-core path splits K
+        S = split_k;
+    }
+    *path = tc ? 1 : 0;
+    *splits = S;
+    return GAI4_OK;
+}
+
+}  // namespace gai4
+
+using namespace gai4;
+
+extern "C" {
+
+int gai4_version(void) { return 100; }
+
+const char* gai4_status_string(int status) {
+    switch (status) {
+    case GAI4_OK: return "ok";
+    case GAI4_ERR_INVALID_ARG: return "invalid argument";
+    case GAI4_ERR_UNSUPPORTED: return "unsupported bits/group_size/dtype/split";
+    case GAI4_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case GAI4_ERR_WORKSPACE: return "split-K workspace missing or too small";
+    case GAI4_ERR_CUDA: return "CUDA error";
+    case GAI4_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    default: return "unknown status";
+    }
+}
+
+gai4_status gai4_quantize(const float* w, uint32_t* w_packed, void* scales, void* biases, gai4_dtype dtype,
+                          int bits, int group_size, int64_t N, int64_t K, void* stream) {
+    gai4_status st = check_affine_shape(dtype, bits, group_size, N, K);
+    if (st != GAI4_OK) return st;
+    if (!w || !w_packed || !scales || !biases) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(w_packed)) return GAI4_ERR_MISALIGNED;
+    return from_cuda(launch_quantize(w, w_packed, scales, biases, dtype, bits, group_size, N, K,
+                                     (cudaStream_t)stream));
+}
+
+gai4_status gai4_unpack(const uint32_t* w_packed, uint8_t* q_out, int bits, int64_t N, int64_t K, void* stream) {
+    if (!valid_bits(bits)) return GAI4_ERR_UNSUPPORTED;
+    if (!w_packed || !q_out || N <= 0 || K <= 0 || (K * bits) % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    return from_cuda(launch_unpack(w_packed, q_out, bits, N, K, (cudaStream_t)stream));
+}
+
+gai4_status gai4_dequantize(const uint32_t* w_packed, const void* scales, const void* biases, float* w_out,
+                            gai4_dtype dtype, int bits, int group_size, int64_t N, int64_t K, void* stream) {
+    gai4_status st = check_affine_shape(dtype, bits, group_size, N, K);
+    if (st != GAI4_OK) return st;
+    if (!w_packed || !scales || !biases || !w_out) return GAI4_ERR_INVALID_ARG;
+    return from_cuda(launch_dequantize(w_packed, scales, biases, w_out, dtype, bits, group_size, N, K,
+                                       (cudaStream_t)stream));
+}
+
+gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* biases, const void* x, void* out,
+                     gai4_dtype dtype, int bits, int group_size, int64_t N, int64_t K, void* stream) {
+    gai4_status st = check_affine_shape(dtype, bits, group_size, N, K);
+    if (st != GAI4_OK) return st;
+    if (!w_packed || !scales || !biases || !x || !out) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(w_packed) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    const AffineGemvLaunch L = plan_affine(w_packed, scales, biases, x, out, bits, group_size, 1, N, K);
+    return from_cuda(launch_affine(L, dtype, (cudaStream_t)stream));
+}
+
+size_t gai4_qmm_t_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits, int group_size, gai4_dtype dtype,
+                                  int split_k) {
+    int path = 0, splits = 1;
+    if (plan_qmm(M, N, K, bits, group_size, dtype, split_k, 0, true, &path, &splits) != GAI4_OK) return 0;
+    return splits > 1 ? (size_t)splits * (size_t)M * (size_t)N * sizeof(float) : 0;
+}
+
+gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group_size, gai4_dtype dtype,
+                            int split_k, size_t workspace_bytes, int* path, int* splits) {
+    if (!path || !splits) return GAI4_ERR_INVALID_ARG;
+    return plan_qmm(M, N, K, bits, group_size, dtype, split_k, workspace_bytes, false, path, splits);
+}
+
+gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void* biases, const void* x, void* out,
+                       gai4_dtype dtype, int bits, int group_size, int64_t M, int64_t N, int64_t K, int split_k,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    int path = 0, splits = 1;
+    gai4_status st = plan_qmm(M, N, K, bits, group_size, dtype, split_k, workspace ? workspace_bytes : 0, false,
+                              &path, &splits);
+    if (st != GAI4_OK) return st;
+    if (!w_packed || !scales || !biases || !x || !out) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(w_packed) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    if (splits > 1) {
+        if (!workspace || workspace_bytes < (size_t)splits * (size_t)M * (size_t)N * sizeof(float))
+            return GAI4_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return GAI4_ERR_MISALIGNED;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (path == 0) {
+        const AffineGemvLaunch L = plan_affine(w_packed, scales, biases, x, out, bits, group_size, M, N, K);
+        return from_cuda(launch_affine(L, dtype, s));
+    }
+    QmmTcLaunch T;
+    T.w = w_packed;
+    T.scales = scales;
+    T.biases = biases;
+    T.x = x;
+    T.out = out;
+    T.partials = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    T.M = M;
+    T.N = N;
+    T.K = K;
+    T.bits = bits;
+    T.group_size = group_size;
+    T.splits = splits;
+    T.is_bf16 = dtype == GAI4_BF16;
+    T.status = status_ptr();
+    T.spin_limit = 1LL << 26;
+    if (!T.status) return GAI4_ERR_CUDA;
+    cudaError_t e = launch_qmm_tc(T, s);
+    if (e != cudaSuccess) return GAI4_ERR_CUDA;
+    if (splits > 1) e = launch_splitk_reduce(T.partials, out, M, N, splits, dtype, s);
+    return from_cuda(e);
+}
+
+gai4_status gai4_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K, void* stream) {
+    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    return from_cuda(launch_q8_0_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
+}
+
+gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K, void* stream) {
+    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 256 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    return from_cuda(launch_q4_k_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
+}
+
+gai4_status gai4_last_device_status(void* stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GAI4_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return GAI4_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return GAI4_ERR_CUDA;
+    }
+    return v == 0 ? GAI4_OK : (gai4_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// internal.h -- launcher interfaces between the C ABI (api.cu) and the kernel
+// translation units. Host-only declarations; no CUDA types beyond cudaStream_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gai4.h"
+
+namespace gai4 {
+
+// CUDA-core affine GEMV / small-M GEMM (affine_gemv_*.cu)
+struct AffineGemvLaunch {
+    const uint32_t* w;
+    const void* scales;
+    const void* biases;
+    const void* x;      // [M, K]
+    void* out;          // [M, N]
+    int64_t M, N, K;
+    int bits, group_size;
+    int ksplit;         // warps of one CTA sharing a row group along K (1, 2, 4 or 8)
+    int rows_per_warp;  // chosen by the launcher
+    int mb;             // x rows per CTA (1, 2, 4, 8)
+};
+cudaError_t launch_affine_gemv_bf16(const AffineGemvLaunch& L, cudaStream_t s);
+cudaError_t launch_affine_gemv_f16(const AffineGemvLaunch& L, cudaStream_t s);
+cudaError_t launch_affine_gemv_f32(const AffineGemvLaunch& L, cudaStream_t s);
+
+// tensor-core qmm_t (qmm_tc.cu)
+struct QmmTcLaunch {
+    const uint32_t* w;
+    const void* scales;
+    const void* biases;
+    const void* x;      // [M, K] bf16/f16
+    void* out;          // [M, N]
+    float* partials;    // [S, M, N] fp32 when splits > 1
+    int64_t M, N, K;
+    int bits, group_size;
+    int splits;
+    int is_bf16;
+    int* status;        // device status word
+    long long spin_limit;
+};
+cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t s);
+int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int group_size);
+
+// quantize / unpack / dequantize (quant.cu)
+cudaError_t launch_quantize(const float* w, uint32_t* packed, void* scales, void* biases,
+                            int dtype, int bits, int gs, int64_t N, int64_t K, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* packed, uint8_t* q, int bits, int64_t N, int64_t K,
+                          cudaStream_t s);
+cudaError_t launch_dequantize(const uint32_t* packed, const void* scales, const void* biases,
+                              float* out, int dtype, int bits, int gs, int64_t N, int64_t K,
+                              cudaStream_t s);
+
+// split-K reduce (qmm_tc.cu): out[m, n] = T(sum_s partials[s, m, n])
+cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N,
+                                 int splits, int dtype, cudaStream_t s);
+
+// block-quantized GEMVs (blockq.cu)
+cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N,
+                             int64_t K, cudaStream_t s);
+cudaError_t launch_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N,
+                             int64_t K, cudaStream_t s);
+
+int num_sms();  // SM count of the current device (cached)
+
+}  // namespace gai4

@@ -1,0 +1,187 @@
+/*
+ * gai4.h -- C ABI of the GB300 (sm_103a) affine group-quantized GEMV / small-M
+ * GEMM library (libgai4.so).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor arguments are DEVICE pointers to caller-owned memory (cudaMalloc,
+ *    PyTorch, ...). The library never frees or keeps them past the call.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). The library allocates no device memory per call; its only
+ *    device-side state is one status word per device (see
+ *    gai4_last_device_status), a static __device__ variable.
+ *  - Arguments are validated on the host before anything is launched. A call
+ *    that returns anything but GAI4_OK has launched nothing and written nothing.
+ *  - Outputs are fully overwritten (no accumulate-into mode).
+ *  - Row-major layouts throughout. "T" is the activation / scale dtype given by
+ *    `dtype`: GAI4_F32 (float), GAI4_F16 (IEEE binary16) or GAI4_BF16.
+ *  - Nothing here aborts, traps or throws; errors are status codes.
+ *
+ * Affine group quantization (metaltile-std quantized.rs, kernel mt_qmv; MLX PR
+ * "[Metal] Add staged affine_qmm_t_nax kernels with split-k", reproduction
+ * script): a weight matrix W [N, K] is cut along K into groups of `group_size`
+ * consecutive elements of one row. Each group stores a scale s and a bias b
+ * (dtype T, arrays [N, K/group_size]) and one unsigned code q in
+ * [0, 2^bits - 1] per element; the represented weight is w = s*q + b. Codes of
+ * one row form a little-endian bit stream: bit j of code k is stream bit
+ * k*bits + j, i.e. bit (k*bits+j)%32 of word (k*bits+j)/32 of the row
+ * (for bits = 4: nibble j of word i is element 8i + j, low nibble first).
+ * The packed matrix is u32 [N, K*bits/32]. Supported: bits in {2,3,4,6,8},
+ * group_size in {32,64,128}; K must be a multiple of group_size.
+ */
+#ifndef GAI4_H
+#define GAI4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gai4_status {
+    GAI4_OK = 0,
+    GAI4_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, K not a multiple of the group/block */
+    GAI4_ERR_UNSUPPORTED = 2,   /* bits / group_size / dtype / split_k outside the supported set */
+    GAI4_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    GAI4_ERR_WORKSPACE = 4,     /* split-K workspace missing or too small for the requested split */
+    GAI4_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+    GAI4_ERR_TIMEOUT = 6        /* a bounded in-kernel wait gave up (reported by gai4_last_device_status) */
+} gai4_status;
+
+typedef enum gai4_dtype {
+    GAI4_F32 = 0,
+    GAI4_F16 = 1,
+    GAI4_BF16 = 2
+} gai4_dtype;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int gai4_version(void);
+
+/* Static text for a status code. Never NULL. */
+const char* gai4_status_string(int status);
+
+/*
+ * gai4_quantize -- affine group quantize/pack W.
+ *   w        [N, K] float32 (device)
+ *   w_packed [N, K*bits/32] u32 (device, 16-byte aligned), fully written
+ *   scales, biases  [N, K/group_size] T (device), fully written
+ * Per group (MLX PR reproduction script, mx.quantize(w, group_size, bits);
+ * bias = min, scale = (max - min)/(2^bits - 1)):
+ *   s  = (max - min) / (2^bits - 1) in binary32, stored as s' = RNE_T(s)
+ *   b' = RNE_T(min)
+ *   q  = clamp(rint((w - b') / s'), 0, 2^bits - 1), binary32 IEEE division,
+ *        round-half-even; q = 0 for the whole group when s' == 0.
+ * The codes are computed from the stored (rounded) s', b'. Bit-exact with the
+ * CPU oracle.
+ */
+gai4_status gai4_quantize(const float* w, uint32_t* w_packed, void* scales, void* biases,
+                          gai4_dtype dtype, int bits, int group_size,
+                          int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_unpack -- codes of a packed matrix: q_out [N, K] uint8 (device),
+ * q_out[n*K + k] = code of element (n, k). Test aid for the bit order.
+ */
+gai4_status gai4_unpack(const uint32_t* w_packed, uint8_t* q_out, int bits,
+                        int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_dequantize -- w_out [N, K] float32 (device):
+ *   w_out[n, k] = RN_f32(s'[n, g] * q[n, k] + b'[n, g]), g = k / group_size
+ * (one rounding of the exact value). Test aid.
+ */
+gai4_status gai4_dequantize(const uint32_t* w_packed, const void* scales, const void* biases,
+                            float* w_out, gai4_dtype dtype, int bits, int group_size,
+                            int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_qmv -- affine quantized matrix-vector product
+ * (metaltile-std quantized.rs, mt_qmv):
+ *   out[n] = sum_g ( s[n,g] * sum_{k in g} q[n,k] x[k] + b[n,g] * sum_{k in g} x[k] )
+ *          = sum_k (s[n,k/gs] q[n,k] + b[n,k/gs]) x[k]
+ *   w_packed [N, K*bits/32] u32; scales, biases [N, K/group_size] T; x [K] T;
+ *   out [N] T. Accumulation in binary32, one rounding to T at the end.
+ *   w_packed and x must be 16-byte aligned (GAI4_ERR_MISALIGNED otherwise).
+ *   Any N >= 1; K a multiple of group_size.
+ */
+gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* biases,
+                     const void* x, void* out, gai4_dtype dtype, int bits, int group_size,
+                     int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_qmm_t -- transposed affine quantized matmul (MLX PR above,
+ * quantized_matmul(x, wq, scales, biases, transpose=True)):
+ *   out[m, n] = sum_k x[m, k] * (s[n,k/gs] q[n,k] + b[n,k/gs]),  m < M, n < N
+ *   x [M, K] T, out [M, N] T, weights as in gai4_qmv.
+ * M = 1 is gai4_qmv. Small M runs a register-tiled CUDA-core kernel; larger M
+ * (bf16 / f16) runs a tensor-core kernel (tcgen05, accumulators in TMEM) that
+ * rounds each dequantized weight once to T before the multiply.
+ * Split-K (MLX PR: K cut into at most 4 ranges of >= 256 columns, K < 512
+ * unsplit, fp32 partials summed by a separate kernel, one rounding after the
+ * sum): split_k = 0 lets the library choose; 1..4 forces that split, which
+ * must give K ranges that are multiples of 64 and of group_size and at least
+ * 256 long (GAI4_ERR_UNSUPPORTED otherwise). With split S > 1 the fp32
+ * partials [S, M, N] live in `workspace` (device, 16-byte aligned,
+ * workspace_bytes >= gai4_qmm_t_workspace_bytes(...) for that split). In
+ * automatic mode the split is also limited to what `workspace_bytes` holds
+ * (workspace may be NULL: no split). The summation order is fixed, so a
+ * given split gives bit-identical results run to run.
+ */
+gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void* biases,
+                       const void* x, void* out, gai4_dtype dtype, int bits, int group_size,
+                       int64_t M, int64_t N, int64_t K, int split_k,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of split-K workspace gai4_qmm_t needs for these arguments (split_k as
+ * passed to gai4_qmm_t; 0 = the automatic choice with unlimited workspace).
+ * 0 when no split is used. */
+size_t gai4_qmm_t_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                                  gai4_dtype dtype, int split_k);
+
+/* The plan gai4_qmm_t would run: *path = 0 (CUDA-core kernel) or 1 (tensor
+ * core), *splits = K split count. workspace_bytes as for gai4_qmm_t.
+ * Returns the status gai4_qmm_t would return for a shape/argument error. */
+gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                            gai4_dtype dtype, int split_k, size_t workspace_bytes,
+                            int* path, int* splits);
+
+/*
+ * gai4_q8_0_gemv -- Q8_0 block-quantized matrix-vector product
+ * (hanzo-kernel quant.rs, matvec_q8 and "Q8_0 PACKED matvec"):
+ *   out[n] = sum_b d[n,b] * sum_{j<32} q[n,b,j] * x[32b + j]
+ *   blocks [N, K/32, 9] u32: word 0 low half = f16 scale d (high half
+ *   ignored), words 1..8 = 32 signed int8 codes, four per word, byte 0 of
+ *   word 1 first. x [K] float32, out [N] float32. K a multiple of 32.
+ *   blocks and x 16-byte aligned.
+ */
+gai4_status gai4_q8_0_gemv(const uint32_t* blocks, const float* x, float* out,
+                           int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_q4_k_gemv -- Q4_K super-block matrix-vector product
+ * (hanzo-kernel quant.rs, Q4_K section, matvec_q4k):
+ *   blocks [N, K/256, 144] bytes: d (f16, bytes 0-1, little-endian), dmin
+ *   (f16, bytes 2-3), 12 scale bytes holding eight 6-bit (sc, m) pairs
+ *   (get_scale_min_k4), 128 qs bytes. For g < 4, i < 32, qb = qs[32g+i]:
+ *     w[64g+i]    = d*sc[2g]*(qb & 15) - dmin*m[2g]
+ *     w[64g+32+i] = d*sc[2g+1]*(qb >> 4) - dmin*m[2g+1]
+ *   out[n] = sum_k w[n,k] x[k]; x [K] float32, out [N] float32.
+ *   K a multiple of 256; blocks and x 16-byte aligned.
+ */
+gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out,
+                           int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_last_device_status -- synchronizes `stream`, then reads and clears the
+ * current device's status word. Returns GAI4_OK, or GAI4_ERR_TIMEOUT if a
+ * bounded wait inside a kernel gave up since the last read (that kernel's
+ * output is then undefined), or GAI4_ERR_CUDA if the synchronization failed.
+ */
+gai4_status gai4_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GAI4_H */

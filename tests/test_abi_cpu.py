@@ -1,0 +1,106 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_affine_int4_gb300 as g4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gai4.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gai4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(g4.LIB_PATH):
+        from gemm_affine_int4_gb300 import build
+        build.build()
+    return g4.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("gai4_qmv", "gai4_qmm_t", "gai4_quantize", "gai4_q8_0_gemv", "gai4_q4_k_gemv"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the Python binding knows the signature of each
+    assert sorted(g4.SIGNATURES) == _declared()
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        s = g4.gai4_status_string(st)
+        assert s and s != "unknown status"
+    assert g4.gai4_status_string(99) == "unknown status"
+    assert g4.gai4_version() >= 100
+
+
+P = ctypes.c_void_p
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_rejects_bad_arguments_without_launching(lib):
+    A = _fake()
+    # null pointers
+    assert lib.gai4_qmv(None, A, A, A, A, 2, 4, 64, 16, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    # K not a multiple of the group size
+    assert lib.gai4_qmv(A, A, A, A, A, 2, 4, 64, 16, 96, None) == g4.GAI4_ERR_INVALID_ARG
+    # unsupported width / group size / dtype
+    assert lib.gai4_qmv(A, A, A, A, A, 2, 5, 64, 16, 64, None) == g4.GAI4_ERR_UNSUPPORTED
+    assert lib.gai4_qmv(A, A, A, A, A, 2, 4, 48, 16, 96, None) == g4.GAI4_ERR_UNSUPPORTED
+    assert lib.gai4_qmv(A, A, A, A, A, 7, 4, 64, 16, 64, None) == g4.GAI4_ERR_UNSUPPORTED
+    # non-positive sizes
+    assert lib.gai4_qmv(A, A, A, A, A, 2, 4, 64, 0, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    # misaligned weights / activations
+    assert lib.gai4_qmv(_fake(0x10004), A, A, A, A, 2, 4, 64, 16, 64, None) == g4.GAI4_ERR_MISALIGNED
+    assert lib.gai4_qmv(A, A, A, _fake(0x10002), A, 2, 4, 64, 16, 64, None) == g4.GAI4_ERR_MISALIGNED
+    # block formats
+    assert lib.gai4_q8_0_gemv(A, A, A, 4, 48, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q4_k_gemv(A, A, A, 4, 300, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q4_k_gemv(_fake(0x10008), A, A, 4, 256, None) == g4.GAI4_ERR_MISALIGNED
+    assert lib.gai4_quantize(A, None, A, A, 2, 4, 64, 4, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    # qmm_t: forced illegal split, too-small workspace
+    assert lib.gai4_qmm_t(A, A, A, A, A, 2, 4, 64, 32, 256, 256, 2, A, 1 << 30, None) == g4.GAI4_ERR_UNSUPPORTED
+    assert lib.gai4_qmm_t(A, A, A, A, A, 2, 4, 64, 0, 256, 256, 0, None, 0, None) == g4.GAI4_ERR_INVALID_ARG
+
+
+def test_split_rules(lib):
+    plan = g4.gai4_qmm_t_plan
+    import torch
+    bf = torch.bfloat16
+    # K < 512 is never split
+    with pytest.raises(g4.Gai4Error):
+        plan(40, 4096, 256, 4, 64, bf, split_k=2, workspace_bytes=1 << 30)
+    # a forced split must give ranges that are multiples of 64 and >= 256 long
+    with pytest.raises(g4.Gai4Error):
+        plan(40, 4096, 640, 4, 64, bf, split_k=4, workspace_bytes=1 << 30)   # 160-long ranges
+    with pytest.raises(g4.Gai4Error):
+        plan(40, 4096, 5 * 64 * 3, 4, 64, bf, split_k=2, workspace_bytes=1 << 30)  # 480: not a multiple of 128
+    # f32 never takes the tensor-core path and never splits
+    assert plan(64, 4096, 4096, 4, 64, torch.float32) == (0, 1)
+    # no workspace, automatic: no split
+    assert plan(64, 4096, 4096, 4, 64, bf, 0, 0)[1] == 1
+    # workspace bytes match the split
+    assert g4.gai4_qmm_t_workspace_bytes(8, 100, 4096, 4, 64, torch.float32, 1) == 0
+
+
+def test_binding_requires_cuda_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        g4.gai4_qmv(torch.zeros(4, 8, dtype=torch.int32), torch.zeros(4, 1), torch.zeros(4, 1), torch.zeros(64),
+                    bits=4, group_size=64)

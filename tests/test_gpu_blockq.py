@@ -1,0 +1,85 @@
+"""GPU Q8_0 / Q4_K GEMVs against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gemm_affine_int4_gb300 as g4
+import oracle
+import synth
+from gpu_util import sample_rows, to_dev
+from tolerance import assert_within
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (5, 96), (67, 1024 + 32), (129, 4096), (33, 14336 + 256)])
+def test_q8_0_small(N, K):
+    blocks = synth.q8_0_blocks(N, K, seed=N + K)
+    x = synth.f32_vector(K, seed=K)
+    ref, absdot = oracle.q8_0_gemv(blocks, x)
+    got = g4.gai4_q8_0_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert_within(got, ref, absdot, "f32", f"q8_0 N={N} K={K}")
+
+
+def test_q8_0_extreme_codes_and_scales():
+    """All 256 byte values, and f16 scales that are subnormal, large or zero."""
+    N, K = 16, 256
+    blocks = synth.q8_0_blocks(N, K, seed=1)
+    allbytes = np.arange(256, dtype=np.uint8).reshape(8, 32)
+    blocks[:8, :, 1:] = allbytes.copy().view("<u4").reshape(8, 1, 8)
+    blocks[8, :, 0] = 0x0001          # smallest f16 subnormal
+    blocks[9, :, 0] = 0x7BFF          # largest finite f16
+    blocks[10, :, 0] = 0x0000         # zero scale
+    blocks[11, :, 0] |= 0xFFFF0000    # junk in the unused high half
+    x = synth.f32_vector(K, seed=2)
+    ref, absdot = oracle.q8_0_gemv(blocks, x)
+    got = g4.gai4_q8_0_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert_within(got, ref, absdot, "f32", "q8_0 extremes")
+
+
+def test_q8_0_closed_form():
+    """q = 1 and x = 1: out = 32 * sum(d) (exact for these sizes in binary32)."""
+    N, K = 8, 256
+    blocks = synth.q8_0_blocks(N, K, seed=3)
+    blocks[:, :, 1:] = 0x01010101
+    d = oracle.to_f64((blocks[:, :, 0] & 0xFFFF).astype(np.uint16), "f16")
+    got = g4.gai4_q8_0_gemv(to_dev(blocks), torch.ones(K, device="cuda")).cpu().numpy()
+    np.testing.assert_allclose(got, 32 * d.sum(axis=1), rtol=1e-5)
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (67, 4096 + 256), (129, 5120)])
+def test_q4_k_small(N, K):
+    blocks = synth.q4_k_blocks(N, K, seed=N + K)
+    x = synth.f32_vector(K, seed=K + 1)
+    ref, absdot = oracle.q4_k_gemv(blocks, x)
+    got = g4.gai4_q4_k_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert_within(got, ref, absdot, "f32", f"q4_k N={N} K={K}")
+
+
+def test_q4_k_element_order_one_hot():
+    """x = e_k picks weight k of every row: checks the nibble / sub-block order."""
+    N, K = 4, 256
+    blocks = synth.q4_k_blocks(N, K, seed=11)
+    w = np.stack([oracle.q4_k_dequant_block(blocks[n, 0]) for n in range(N)])
+    for k in (0, 1, 31, 32, 63, 64, 100, 129, 175, 200, 255):
+        x = np.zeros(K, np.float32)
+        x[k] = 1.0
+        got = g4.gai4_q4_k_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(got, w[:, k], rtol=2e-6, atol=1e-7, err_msg=f"k={k}")
+
+
+@pytest.mark.parametrize("kind,N,K,seed", [("q8_0", 4096, 4096, 300), ("q8_0", 14336, 5120, 301),
+                                           ("q4_k", 4096, 4096, 302), ("q4_k", 14336, 5120, 303)])
+def test_blockq_full_size_sampled(kind, N, K, seed):
+    x = synth.f32_vector(K, seed + 1)
+    rows = sample_rows(N, 128, seed)
+    if kind == "q8_0":
+        blocks = synth.q8_0_blocks(N, K, seed)
+        got = g4.gai4_q8_0_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+        ref, absdot = oracle.q8_0_gemv(blocks, x, rows=rows)
+    else:
+        blocks = synth.q4_k_blocks(N, K, seed)
+        got = g4.gai4_q4_k_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+        ref, absdot = oracle.q4_k_gemv(blocks, x, rows=rows)
+    assert_within(got[rows], ref, absdot, "f32", f"{kind} {N}x{K}")
+    assert np.all(np.isfinite(got))
