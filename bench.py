@@ -168,7 +168,15 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def build_workload(torch, g4, dev, seed=0):
+def selected(only, fam, idx):
+    """--only FAMILY[:INDEX] restricts the workload (profiling runs)."""
+    if not only:
+        return True
+    f, _, i = only.partition(":")
+    return f == fam and (i == "" or int(i) == idx)
+
+
+def build_workload(torch, g4, dev, seed=0, only=None):
     """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
     blocks from the shared seeded generators."""
@@ -184,13 +192,17 @@ def build_workload(torch, g4, dev, seed=0):
         del w
         return p, s, b
 
-    for N, K in QMV_SHAPES:
+    for i, (N, K) in enumerate(QMV_SHAPES):
+        if not selected(only, "qmv", i):
+            continue
         p, s, b = qweights(N, K)
         x = torch.randn((K,), generator=gen, device=dev).to(bf)
         out = torch.empty((N,), dtype=bf, device=dev)
         calls["qmv"].append(dict(kind="qmv", p=p, s=s, b=b, x=x, out=out, M=1, N=N, K=K,
                                  bytes=affine_bytes(1, N, K)))
-    for K, N, M in QMM_SHAPES:
+    for i, (K, N, M) in enumerate(QMM_SHAPES):
+        if not selected(only, "qmm_t", i):
+            continue
         p, s, b = qweights(N, K)
         x = torch.randn((M, K), generator=gen, device=dev).to(bf)
         out = torch.empty((M, N), dtype=bf, device=dev)
@@ -199,16 +211,18 @@ def build_workload(torch, g4, dev, seed=0):
         calls["qmm_t"].append(dict(kind="qmm_t", p=p, s=s, b=b, x=x, out=out, ws=wsp, M=M, N=N, K=K,
                                    bytes=affine_bytes(M, N, K)))
     for i, (N, K) in enumerate(BLOCKQ_SHAPES):
-        blk8 = torch.from_numpy(synth.q8_0_blocks(N, K, 300 + i).view(np.int32)).to(dev)
-        blk4 = torch.from_numpy(synth.q4_k_blocks(N, K, 302 + i)).to(dev)
-        x8 = torch.from_numpy(synth.f32_vector(K, 301 + i)).to(dev)
-        x4 = torch.from_numpy(synth.f32_vector(K, 303 + i)).to(dev)
-        calls["q8_0"].append(dict(kind="q8_0", blocks=blk8, x=x8, out=torch.empty(N, device=dev), N=N, K=K,
-                                  bytes=q8_bytes(N, K)))
-        calls["q4_k"].append(dict(kind="q4_k", blocks=blk4, x=x4, out=torch.empty(N, device=dev), N=N, K=K,
-                                  bytes=q4k_bytes(N, K)))
+        if selected(only, "q8_0", i):
+            blk8 = torch.from_numpy(synth.q8_0_blocks(N, K, 300 + i).view(np.int32)).to(dev)
+            x8 = torch.from_numpy(synth.f32_vector(K, 301 + i)).to(dev)
+            calls["q8_0"].append(dict(kind="q8_0", blocks=blk8, x=x8, out=torch.empty(N, device=dev), N=N, K=K,
+                                      bytes=q8_bytes(N, K)))
+        if selected(only, "q4_k", i):
+            blk4 = torch.from_numpy(synth.q4_k_blocks(N, K, 302 + i)).to(dev)
+            x4 = torch.from_numpy(synth.f32_vector(K, 303 + i)).to(dev)
+            calls["q4_k"].append(dict(kind="q4_k", blocks=blk4, x=x4, out=torch.empty(N, device=dev), N=N, K=K,
+                                      bytes=q4k_bytes(N, K)))
     torch.cuda.synchronize()
-    return calls
+    return {f: cs for f, cs in calls.items() if cs}
 
 
 def issue(g4, c):
@@ -244,7 +258,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     g4.lib()
-    calls = build_workload(torch, g4, dev)
+    calls = build_workload(torch, g4, dev, only=args.only)
     fam_bytes = {f: sum(c["bytes"] for c in cs) for f, cs in calls.items()}
     total_bytes = sum(fam_bytes.values())
     stream = torch.cuda.Stream(device=dev)
@@ -320,7 +334,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the public API: per step, H2D of every call's
     # activations from pinned host memory, the calls, D2H of every output
-    e2e = run_e2e(torch, g4, calls, stream, args)
+    e2e = None if args.no_e2e else run_e2e(torch, g4, calls, stream, args)
 
     ms_per_step = elapsed_ms / steps_total
     if world > 1:
@@ -509,6 +523,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", default=None, help="FAMILY[:INDEX]: time one kernel family / call (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -240,7 +240,7 @@ gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void*
     T.splits = splits;
     T.is_bf16 = dtype == GAI4_BF16;
     T.status = status_ptr();
-    T.spin_limit = 1LL << 26;
+    T.spin_limit = 2000000000LL;   // ~1 s of SM clock per wait
     if (!T.status) return GAI4_ERR_CUDA;
     cudaError_t e = launch_qmm_tc(T, s);
     if (e != cudaSuccess) return GAI4_ERR_CUDA;

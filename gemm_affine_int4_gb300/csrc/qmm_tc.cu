@@ -1,4 +1,39 @@
-// qmm_tc.cu -- tensor-core qmm_t and the split-K reduce (sm_103a).
+// qmm_tc.cu -- tensor-core qmm_t (sm_103a: TMA, mbarrier, tcgen05 / TMEM) and
+// the split-K reduce.
+//
+// out[m, n] = sum_k x[m, k] * w_hat[n, k], w_hat = s * q + b (MLX PR "[Metal]
+// Add staged affine_qmm_t_nax kernels with split-k": transposed affine
+// quantized_matmul, split-K with fp32 partials and a separate accumulate
+// kernel; metaltile-std quantized.rs, mt_qmm_mma: dequantize the weight tile
+// once, then run the matrix unit on it).
+//
+// Mapping ("swap AB"): the 128 rows of a weight tile are the MMA M dimension,
+// the x rows (tokens, padded to a multiple of 16) are the MMA N dimension, so a
+// few tokens still make a legal tcgen05 shape and the accumulator
+// D[128 x Mt] (fp32) lives in tensor memory.
+//
+// One CTA = one 128-row weight tile x one K range (split) x one chunk of at
+// most 256 x rows. Warp roles:
+//   warp 0      TMA producer of the packed-weight tiles (ring of kWStages)
+//   warp 1      TMA producer of the activation tiles (ring of kXStages),
+//               128-byte swizzled = the canonical K-major UMMA layout
+//   warp 2      MMA issuer (one thread): tcgen05.mma kind::f16, A operand
+//               from tensor memory, B operand (activations) from shared memory
+//   warp 3      idle (keeps the warp count a multiple of 4)
+//   warps 4-11  dequantize: thread t of warp quadrant q owns weight row
+//               32q + t and half of the stage's 128 K columns; it decodes the
+//               codes, computes w_hat = fma(q, s, b) in bf16x2/f16x2 (one
+//               rounding of the exact value) and stores the row slice straight
+//               into tensor memory with tcgen05.st (the A ring, kAStages), so
+//               the weights never pass through shared memory a second time.
+//               After the K loop the same warps read the accumulator
+//               (tcgen05.ld) and write fp32 partials or the rounded output.
+// Every wait on an mbarrier is bounded; on time-out the kernel records
+// GAI4_ERR_TIMEOUT in the device status word, lets the other roles drain, frees
+// its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,8 +88,567 @@ cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, in
     return cudaGetLastError();
 }
 
-int qmm_tc_supported(int64_t, int64_t, int64_t, int, int) { return 0; }
+// ---------------------------------------------------------------------------
+// tensor-core kernel
+// ---------------------------------------------------------------------------
+namespace tc {
 
-cudaError_t launch_qmm_tc(const QmmTcLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kTileN = 128;      // weight rows per CTA (MMA M)
+constexpr int kBK = 128;         // K columns per pipeline stage
+constexpr int kMaxWStages = 12;  // packed-weight ring (runtime depth <= this)
+constexpr int kAStages = 2;      // tensor-memory A ring (64 columns each)
+constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
+// 12 warps: a multiple of 4, so that warp w of every co-resident CTA runs on
+// SM sub-partition w % 4 and reaches tensor-memory lanes 32 (w % 4) .. +31
+constexpr int kThreads = 32 * 12;
+constexpr int kDequantWarp0 = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+struct Ctl {
+    int* status;            // device status word
+    long long limit;        // clock64 cycles a single wait may take
+    volatile int* abort_;   // shared flag: some role gave up
+};
+
+// bounded wait: false after `limit` cycles (or when another role gave up)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*c.abort_) return false;
+        if (clock64() - t0 > c.limit) {
+            *c.abort_ = 1;
+            atomicExch(c.status, (int)GAI4_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// bounded wait that ignores the abort flag: used to drain copies and MMAs that
+// were already issued, so that no asynchronous write lands after the CTA exits
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) {
+            atomicExch(status, (int)GAI4_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// warp-uniform wait: lane 0 spins, the warp then reconverges (the following
+// tcgen05 .sync.aligned instructions need every lane, converged) and takes
+// lane 0's answer
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+    const int lane = threadIdx.x & 31;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, c) ? 1 : 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major, 128-byte swizzled shared-memory operand descriptor (sm_100 UMMA):
+// start address >> 4, leading byte offset (unused for this layout) = 1,
+// stride byte offset = 1024 (8 rows x 128 B), descriptor version 1, layout
+// SWIZZLE_128B (2).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// instruction descriptor, kind::f16: fp32 accumulate, A/B bf16 (1) or f16 (0),
+// both K-major, N = mt, M = 128
+__host__ __device__ constexpr uint32_t make_idesc(int is_bf16, int mt) {
+    return (1u << 4) | ((uint32_t)is_bf16 << 7) | ((uint32_t)is_bf16 << 10) | ((uint32_t)(mt >> 3) << 17) |
+           ((uint32_t)(kTileN >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// packed 16-bit pair arithmetic (one rounding per result)
+template <bool BF>
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (BF)
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+template <bool BF>
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    if constexpr (BF)
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    else
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+struct Params {
+    const uint16_t* scales;
+    const uint16_t* biases;
+    void* out;            // [M, N] T (splits == 1)
+    float* partials;      // [S, M, N] fp32 (splits > 1)
+    int64_t M, N, K;
+    int64_t groups;       // K / group_size
+    int gs_log2;          // log2(group_size)
+    int k_per_split;      // K columns per split (multiple of 64)
+    int splits;
+    int mt;               // MMA N: x rows of this CTA rounded up to 16 (<= 256)
+    int x_stages;
+    int w_stages;
+    int tmem_cols;        // allocated columns (power of two)
+    int* status;
+    long long spin_limit;
+};
+
+// ---------------------------------------------------------------------------
+// 4-bit codes: one 32-bit word (8 codes, low nibble first) -> 4 registers of
+// w_hat pairs (k, k+1) in 16-bit format T.
+// ---------------------------------------------------------------------------
+template <bool BF>
+__device__ __forceinline__ void dequant_word4(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* o) {
+    constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;   // 128.0 / 1024.0 in both halves
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t p = ((w >> (4 * j)) & 0x000F000Fu) | kMagic;   // (C + q_j, C + q_{j+4})
+        const uint32_t q = hsub2<BF>(p, kMagic);                       // (q_j, q_{j+4}) exact
+        r[j] = hfma2<BF>(q, s2, b2);                                   // (w_j, w_{j+4})
+    }
+    o[0] = __byte_perm(r[0], r[1], 0x5410);   // (w0, w1)
+    o[1] = __byte_perm(r[2], r[3], 0x5410);   // (w2, w3)
+    o[2] = __byte_perm(r[0], r[1], 0x7632);   // (w4, w5)
+    o[3] = __byte_perm(r[2], r[3], 0x7632);   // (w6, w7)
+}
+
+template <bool BF>
+__global__ void __launch_bounds__(kThreads, 1)
+    qmm_tc4_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base (128-byte swizzle atoms)
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int mt = p.mt;
+    const int XS = p.x_stages;
+    const int kWStages = p.w_stages;
+    const uint32_t x_stage_bytes = (uint32_t)mt * kBK * 2;     // two 64-column swizzle atoms
+    const uint32_t w_stage_bytes = kTileN * kBK / 2;           // 4-bit codes
+    uint8_t* xbuf = smem;                                      // XS x stages
+    uint8_t* wbuf = xbuf + (size_t)XS * x_stage_bytes;         // kWStages w stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + (size_t)kWStages * w_stage_bytes);
+    uint64_t* w_full = bars;
+    uint64_t* w_empty = w_full + kMaxWStages;
+    uint64_t* x_full = w_empty + kMaxWStages;
+    uint64_t* x_empty = x_full + 4;
+    uint64_t* a_full = x_empty + 4;
+    uint64_t* a_empty = a_full + kAStages;
+    uint64_t* acc_full = a_empty + kAStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n0 = (int64_t)blockIdx.x * kTileN;
+    const int split = blockIdx.y;
+    const int64_t m0 = (int64_t)blockIdx.z * kMaxMt;
+    const int64_t k_begin = (int64_t)split * p.k_per_split;
+    const int nk64 = p.k_per_split / 64;                       // 64-column halves in this split
+    const int nst = (nk64 + 1) / 2;                            // 128-column stages
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWStages; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], 8);          // one arrive per dequant warp
+        }
+        for (int i = 0; i < XS; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);          // tcgen05.commit
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&a_full[i], 8);
+            mbar_init(&a_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {   // tensor-memory allocation (whole warp)
+        __syncwarp();
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t acc_col = 0;                  // accumulator: columns [0, mt)
+    const uint32_t a_col0 = (uint32_t)p.tmem_cols - 64u * kAStages;   // A ring at the top
+    Ctl ctl{p.status, p.spin_limit, abort_flag};
+
+    if (warp == 0) {
+        // ---------------- packed-weight producer ----------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % kWStages;
+                if (!mbar_wait(&w_empty[s], ((i / kWStages) & 1) ^ 1, ctl)) break;
+                mbar_arrive_expect_tx(&w_full[s], w_stage_bytes);
+                // x coordinate in 32-bit words: (k_begin + 128 i) * 4 / 32
+                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)((k_begin + kBK * i) / 8),
+                            (int)n0);
+                ++issued;
+            }
+            // drain: every issued copy has landed before the CTA may exit
+            for (int i = (issued > kWStages ? issued - kWStages : 0); i < issued; ++i)
+                mbar_wait_drain(&w_full[i % kWStages], (i / kWStages) & 1, p.spin_limit, p.status);
+        }
+    } else if (warp == 1) {
+        // ---------------- activation producer ----------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % XS;
+                if (!mbar_wait(&x_empty[s], ((i / XS) & 1) ^ 1, ctl)) break;
+                mbar_arrive_expect_tx(&x_full[s], x_stage_bytes);
+                uint8_t* dst = xbuf + (size_t)s * x_stage_bytes;
+                const int kx = (int)(k_begin + kBK * i);
+                tma_load_2d(dst, &xmap, &x_full[s], kx, (int)m0);
+                tma_load_2d(dst + (size_t)mt * 128, &xmap, &x_full[s], kx + 64, (int)m0);
+                ++issued;
+            }
+            for (int i = (issued > XS ? issued - XS : 0); i < issued; ++i)
+                mbar_wait_drain(&x_full[i % XS], (i / XS) & 1, p.spin_limit, p.status);
+        }
+    } else if (warp == 2) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(BF ? 1 : 0, mt);
+            uint32_t acc_flag = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int sa = i % kAStages, sx = i % XS;
+                if (!mbar_wait(&a_full[sa], (i / kAStages) & 1, ctl)) break;
+                if (!mbar_wait(&x_full[sx], (i / XS) & 1, ctl)) break;
+                fence_after();
+                const int kk_end = (2 * i + 1 < nk64) ? 8 : 4;   // last stage may hold one 64-column half
+                const uint32_t xaddr = smem_u32(xbuf + (size_t)sx * x_stage_bytes);
+                for (int kk = 0; kk < kk_end; ++kk) {
+                    const uint32_t a_t = tmem_base + a_col0 + (uint32_t)sa * 64u + (uint32_t)kk * 8u;
+                    const uint32_t baddr = xaddr + (uint32_t)(kk >> 2) * (uint32_t)mt * 128u + (uint32_t)(kk & 3) * 32u;
+                    mma_f16_tmem_a(tmem_base + acc_col, a_t, sw128_desc(baddr), idesc, acc_flag);
+                    acc_flag = 1;
+                }
+                mma_commit(&a_empty[sa]);
+                mma_commit(&x_empty[sx]);
+            }
+            mma_commit(acc_full);   // completes when every MMA above has finished
+            // no MMA may still run when tensor memory is freed
+            mbar_wait_drain(acc_full, 0, p.spin_limit, p.status);
+        }
+    } else if (warp == 3) {
+        // idle
+    } else {
+        // ---------------- dequantize, then epilogue ----------------
+        const int dw = warp - kDequantWarp0;        // 0..7
+        const int quad = warp & 3;                  // TMEM lane quadrant of this warp
+        const int half = dw >> 2;                   // which 64 of the stage's 128 columns
+        const int r = quad * 32 + lane;             // weight row within the tile
+        const int64_t row = n0 + r;
+        const bool row_ok = row < p.N;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+
+        for (int i = 0; i < nst; ++i) {
+            const int sw = i % kWStages, sa = i % kAStages;
+            const bool active = (2 * i + half) < nk64;   // this half exists in the split
+            if (!warp_wait(&w_full[sw], (i / kWStages) & 1, ctl)) break;
+            // the row's 32 bytes of this half: 64-byte rows, 64-byte TMA swizzle
+            // (16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3))
+            uint32_t wv[8];
+            {
+                const uint8_t* rowp = wbuf + (size_t)sw * w_stage_bytes + (size_t)r * 64;
+                const int sx = (r >> 1) & 3;
+                const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * half) ^ sx));
+                const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * half + 1) ^ sx));
+                wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
+                wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[sw]);
+
+            uint32_t o[32];
+            if (active) {
+                // scale / bias of the (one or two) groups of these 64 columns
+                const int64_t k0 = k_begin + (int64_t)kBK * i + 64 * half;
+                const int64_t g0 = k0 >> p.gs_log2;
+                const int64_t g1 = (k0 + 32) >> p.gs_log2;
+                uint32_t s2a = 0, b2a = 0, s2b = 0, b2b = 0;
+                if (row_ok) {
+                    const uint32_t sa_ = __ldg(p.scales + row * p.groups + g0);
+                    const uint32_t ba_ = __ldg(p.biases + row * p.groups + g0);
+                    const uint32_t sb_ = __ldg(p.scales + row * p.groups + g1);
+                    const uint32_t bb_ = __ldg(p.biases + row * p.groups + g1);
+                    s2a = sa_ | (sa_ << 16);
+                    b2a = ba_ | (ba_ << 16);
+                    s2b = sb_ | (sb_ << 16);
+                    b2b = bb_ | (bb_ << 16);
+                }
+#pragma unroll
+                for (int wi = 0; wi < 8; ++wi) {
+                    if (wi < 4) dequant_word4<BF>(wv[wi], s2a, b2a, &o[4 * wi]);
+                    else dequant_word4<BF>(wv[wi], s2b, b2b, &o[4 * wi]);
+                }
+            }
+            if (!warp_wait(&a_empty[sa], ((i / kAStages) & 1) ^ 1, ctl)) break;
+            fence_after();
+            if (active) {
+                tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 64u + (uint32_t)half * 32u, o);
+                tmem_st_wait();
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sa]);
+        }
+
+        // epilogue: accumulator rows -> fp32 partials or T output
+        const bool ok = warp_wait(acc_full, 0, ctl);
+        fence_after();
+        if (ok) {
+            const int64_t mrows = min((int64_t)mt, p.M - m0);
+            const int cols_half = mt / 2;              // multiple of 8
+            const int c_begin = half * cols_half;
+            for (int c = c_begin; c < c_begin + cols_half; c += 8) {
+                uint32_t v[8];
+                __syncwarp();
+                tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)c, v);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int64_t m = c + j;
+                        if (m < mrows) {
+                            const float f = __uint_as_float(v[j]);
+                            const int64_t idx = (m0 + m) * p.N + row;
+                            if (p.splits > 1) {
+                                p.partials[(int64_t)split * p.M * p.N + idx] = f;
+                            } else if (BF) {
+                                static_cast<uint16_t*>(p.out)[idx] = BF16::from_f32(f);
+                            } else {
+                                static_cast<uint16_t*>(p.out)[idx] = F16::from_f32(f);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using tc::kAStages;
+using tc::kBK;
+using tc::kMaxMt;
+using tc::kThreads;
+using tc::kTileN;
+using tc::kMaxWStages;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int gs) {
+    (void)M;
+    (void)N;
+    if (bits != 4) return 0;
+    if (K % 64 != 0 || gs < 32) return 0;   // 64-column halves, whole groups
+    return 1;
+}
+
+static int pow2_at_least(int v) {
+    int p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t M = L.M, N = L.N, K = L.K;
+    const int S = L.splits;
+    const int64_t kps = K / S;
+    const int64_t mchunks = (M + kMaxMt - 1) / kMaxMt;
+    const int64_t mrows = M < kMaxMt ? M : kMaxMt;
+    const int mt = (int)((mrows + 15) / 16 * 16);
+    const int xs = mt > 128 ? 2 : 3;
+
+    // packed weights: u32 [N, K/8], box {16 words = 128 columns, 128 rows}, 64-byte swizzle
+    CUtensorMap wmap, xmap;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        cuuint32_t box[2] = {16, 128};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(L.w), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // activations: 16-bit [M, K], box {64 columns, mt rows}, 128-byte swizzle
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+        cuuint32_t box[2] = {64, (cuuint32_t)mt};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(L.x), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // One CTA per SM: a second co-resident CTA of this kernel would run warps
+    // whose tensor-memory lane quadrant differs from (warp index % 4), which
+    // the dequantize and epilogue roles rely on. The shared memory request is
+    // therefore kept above half of the SM's capacity; the space goes to a
+    // deeper packed-weight ring.
+    const size_t kBars = 512;
+    const size_t x_bytes = (size_t)xs * mt * kBK * 2;
+    const size_t w_stage = (size_t)kTileN * kBK / 2;
+    const size_t budget = 200 * 1024;
+    int ws = (int)((budget - 1024 - kBars - x_bytes) / w_stage);
+    ws = ws < 4 ? 4 : (ws > kMaxWStages ? kMaxWStages : ws);
+    size_t smem = 1024 + x_bytes + (size_t)ws * w_stage + kBars;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    static_assert((2 * kMaxWStages + 2 * 4 + 2 * 2 + 1) * 8 + 8 <= 512, "barrier area");
+    tc::Params p;
+    p.scales = static_cast<const uint16_t*>(L.scales);
+    p.biases = static_cast<const uint16_t*>(L.biases);
+    p.out = L.out;
+    p.partials = L.partials;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.groups = K / L.group_size;
+    int lg = 0;
+    while ((1 << lg) < L.group_size) ++lg;
+    p.gs_log2 = lg;
+    p.k_per_split = (int)kps;
+    p.splits = S;
+    p.mt = mt;
+    p.x_stages = xs;
+    p.w_stages = ws;
+    p.tmem_cols = pow2_at_least(mt + 64 * kAStages);
+    p.status = L.status;
+    p.spin_limit = L.spin_limit;
+
+
+    auto kern = L.is_bf16 ? tc::qmm_tc4_kernel<true> : tc::qmm_tc4_kernel<false>;
+    static unsigned long long configured[2] = {0ull, 0ull};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int which = L.is_bf16 ? 1 : 0;
+    if (dev >= 64 || !(configured[which] & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured[which] |= 1ull << dev;
+    }
+    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)S, (unsigned)mchunks);
+    kern<<<grid, kThreads, smem, stream>>>(wmap, xmap, p);
+    return cudaGetLastError();
+}
 
 }  // namespace gai4

@@ -1,0 +1,101 @@
+"""GPU qmm_t on the tensor-core path (tcgen05) and split-K against the oracle.
+
+The tensor-core path rounds each dequantized weight once to the 16-bit MMA
+operand type (as the dequantize-then-MMA kernels of metaltile-std
+quantized.rs do); the acceptance bound is the same as everywhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_affine_int4_gb300 as g4
+import oracle
+from gpu_util import TORCH_DTYPE, affine_problem, sample_rows, to_dev, to_host_f64
+from tolerance import assert_within
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(packed, s, b, x, dtype, split_k=0, bits=4, gs=64):
+    M, K = x.shape
+    N = packed.shape[0]
+    ws_bytes = g4.gai4_qmm_t_workspace_bytes(M, N, K, bits, gs, TORCH_DTYPE[dtype], split_k)
+    ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device="cuda") if ws_bytes else None
+    out = g4.gai4_qmm_t(to_dev(packed), to_dev(s, dtype), to_dev(b, dtype), to_dev(x, dtype), bits=bits,
+                        group_size=gs, split_k=split_k, workspace=ws)
+    assert g4.gai4_last_device_status() == 0
+    return out
+
+
+CASES = [(131, 1088, 9), (256, 2048, 16), (300, 1024, 40), (129, 4096, 85), (64, 512, 256), (200, 1024, 300),
+         (1000, 1536, 33)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("N,K,M", CASES)
+def test_tc_matches_oracle_all_splits(N, K, M, dtype):
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, dtype, seed=N + K + M)
+    path, _ = g4.gai4_qmm_t_plan(M, N, K, 4, 64, TORCH_DTYPE[dtype])
+    assert path == 1
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, dtype)
+    for S in (1, 2, 3, 4):
+        try:
+            g4.gai4_qmm_t_plan(M, N, K, 4, 64, TORCH_DTYPE[dtype], split_k=S, workspace_bytes=1 << 40)
+        except g4.Gai4Error:
+            continue   # not a legal split of this K
+        out = _run(packed, s, b, x, dtype, split_k=S)
+        assert_within(to_host_f64(out, dtype), ref, absdot, dtype, f"tc N={N} K={K} M={M} S={S} {dtype}")
+
+
+@pytest.mark.parametrize("gs", [32, 128])
+def test_tc_group_sizes(gs):
+    N, K, M = 192, 2048, 24
+    _, packed, s, b, x = affine_problem(N, K, M, 4, gs, "bf16", seed=gs)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, gs, "bf16")
+    for S in (1, 2, 4):
+        out = _run(packed, s, b, x, "bf16", split_k=S, gs=gs)
+        assert_within(to_host_f64(out, "bf16"), ref, absdot, "bf16", f"tc gs={gs} S={S}")
+
+
+def test_tc_split_deterministic():
+    """A fixed split gives bit-identical outputs run to run (fixed summation order)."""
+    for N, K, M in ((512, 4096, 33), (128, 4096, 48), (640, 2048, 96)):
+        _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=77)
+        for S in (1, 2, 4):
+            a = _run(packed, s, b, x, "bf16", split_k=S)
+            for _ in range(8):
+                c = _run(packed, s, b, x, "bf16", split_k=S)
+                assert torch.equal(a.view(torch.int16), c.view(torch.int16)), (N, K, M, S)
+
+
+def test_tc_rows_equal_qmv():
+    """Each output row of qmm_t agrees with qmv on that x row (both within the bound)."""
+    N, K, M = 256, 2048, 12
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=3)
+    out = to_host_f64(_run(packed, s, b, x, "bf16", split_k=2), "bf16")
+    for m in (0, 5, 11):
+        v = g4.gai4_qmv(to_dev(packed), to_dev(s, "bf16"), to_dev(b, "bf16"), to_dev(x[m], "bf16"))
+        ref, absdot = oracle.qmm(packed, s, b, x[m], 4, 64, "bf16")
+        assert_within(to_host_f64(v, "bf16"), ref, absdot, "bf16", "qmv row")
+        assert_within(out[m], ref, absdot, "bf16", "qmm_t row")
+
+
+# (K, N, M) of the mid-M split-K shapes and the compute-bound control
+FULL = [(2048, 2048, 22), (4096, 4096, 16), (10752, 2048, 85), (14336, 4096, 33), (17408, 5120, 56),
+        (5120, 17408, 28), (256, 4096, 40), (4096, 4096, 512)]
+
+
+@pytest.mark.parametrize("K,N,M", FULL)
+def test_tc_full_size_sampled(K, N, M):
+    seed = 100 + FULL.index((K, N, M))
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=seed)
+    ws_bytes = g4.gai4_qmm_t_workspace_bytes(M, N, K, 4, 64, torch.bfloat16, 0)
+    ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device="cuda")
+    out = g4.gai4_qmm_t(to_dev(packed), to_dev(s, "bf16"), to_dev(b, "bf16"), to_dev(x, "bf16"), bits=4,
+                        group_size=64, split_k=0, workspace=ws)   # the benchmark's call
+    assert g4.gai4_last_device_status() == 0
+    got = to_host_f64(out, "bf16")
+    rows = sample_rows(N, 48, seed)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16", rows=rows)
+    assert_within(got[:, rows], ref, absdot, "bf16", f"qmm_t {K}x{N} M={M}")
+    assert np.all(np.isfinite(got))
