@@ -332,6 +332,8 @@ def run_gpu(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
 
+    per_call = None if args.no_per_call else time_per_call(torch, g4, calls, stream, fams)
+
     # end to end through the public API: per step, H2D of every call's
     # activations from pinned host memory, the calls, D2H of every output
     e2e = None if args.no_e2e else run_e2e(torch, g4, calls, stream, args)
@@ -375,6 +377,7 @@ def run_gpu(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": round(fam_bytes[dom] / n_launch),
                      "avg_launch_us": round(dom_ms * 1e3 / n_launch, 3),
                      "traffic": None if traffic is None else round(traffic / n_launch)},
+        "per_call_cold_l2": per_call,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,
@@ -382,6 +385,43 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return res
+
+
+def call_name(c):
+    if c["kind"] == "qmm_t":
+        return f"qmm_t K{c['K']}xN{c['N']} M={c['M']}"
+    return f"{c['kind']} N{c['N']}xK{c['K']}"
+
+
+def time_per_call(torch, g4, calls, stream, fams, reps=10):
+    """Each call alone (its own CUDA graph), cold L2: a 256 MB buffer is
+    overwritten before every timed replay. Reported beside the step timing."""
+    hbm, _, _ = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=stream.device)
+    out = []
+    for fam in fams:
+        for c in calls[fam]:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                issue(g4, c)
+            ts = []
+            with torch.cuda.stream(stream):
+                for r in range(reps + 2):
+                    flush.fill_(float(r))
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    gr.replay()
+                    e1.record(stream)
+                    ts.append((e0, e1))
+            stream.synchronize()
+            us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts[2:])
+            med = us[len(us) // 2]
+            gbs = c["bytes"] / (med * 1e-6) / 1e9
+            out.append({"call": call_name(c), "us": round(med, 3), "GB/s": round(gbs, 1),
+                        "frac_of_hbm": round(gbs / hbm, 3)})
+    del flush
+    return out
 
 
 def run_e2e(torch, g4, calls, stream, args):
@@ -525,6 +565,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", default=None, help="FAMILY[:INDEX]: time one kernel family / call (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-call", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
