@@ -45,6 +45,7 @@ SIGNATURES = {
     "gai4_qmm_t_workspace_bytes": ([_I64, _I64, _I64, _I, _I, _I, _I], ctypes.c_size_t),
     "gai4_qmm_t_plan": ([_I64, _I64, _I64, _I, _I, _I, _I, ctypes.c_size_t, ctypes.POINTER(_I),
                          ctypes.POINTER(_I)], _I),
+    "gai4_qmm_t_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I64, _I64, _I64, _I, _P], _I),
     "gai4_q8_0_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_q4_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
@@ -184,6 +185,23 @@ def gai4_qmm_t(w_packed, scales, biases, x, out=None, bits: int = 4, group_size:
     _check("gai4_qmm_t", lib().gai4_qmm_t(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x), _ptr(out),
                                           _dtype(x), bits, group_size, M, N, K, split_k, _ptr(workspace),
                                           ws_bytes, _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def gai4_qmm_t_noalloc(w_packed, scales, biases, x, out, bits: int = 4, group_size: int = 64, split_k: int = 0,
+                       stream=None):
+    """gai4_qmm_t without a workspace argument: the split-K partials use the
+    library's fixed 8 MiB device array (for callers that cannot allocate
+    device memory; `out` must be given). Calls that overlap on the GPU race
+    on that array."""
+    M, K = x.shape
+    N = w_packed.shape[0]
+    _check("gai4_qmm_t_noalloc", lib().gai4_qmm_t_noalloc(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x),
+                                                          _ptr(out), _dtype(x), bits, group_size, M, N, K, split_k,
+                                                          _stream(stream)))
     return out
 
 

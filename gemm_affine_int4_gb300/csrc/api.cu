@@ -272,3 +272,37 @@ gai4_status gai4_last_device_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gai4_qmm_t_noalloc: gai4_qmm_t with the split-K partials in a fixed device
+// array of this library, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace gai4 {
+
+static __device__ __align__(256) float g_noalloc_scratch[GAI4_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+// Device address of the array for the current device. In host code
+// g_noalloc_scratch names a host-side stand-in, not device memory, so the
+// address is looked up once per device (that device current) and cached.
+static float* noalloc_scratch() {
+    static float* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<float*>(p);
+    }
+    return ptrs[dev];
+}
+
+}  // namespace gai4
+
+extern "C" gai4_status gai4_qmm_t_noalloc(const uint32_t* w_packed, const void* scales, const void* biases,
+                                          const void* x, void* out, gai4_dtype dtype, int bits, int group_size,
+                                          int64_t M, int64_t N, int64_t K, int split_k, void* stream) {
+    float* scratch = gai4::noalloc_scratch();
+    if (!scratch) return GAI4_ERR_CUDA;
+    return gai4_qmm_t(w_packed, scales, biases, x, out, dtype, bits, group_size, M, N, K, split_k, scratch,
+                      (size_t)GAI4_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -7,9 +7,10 @@
  *  - All tensor arguments are DEVICE pointers to caller-owned memory (cudaMalloc,
  *    PyTorch, ...). The library never frees or keeps them past the call.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
- *    default stream). The library allocates no device memory per call; its only
+ *    default stream). The library allocates no device memory per call; its
  *    device-side state is one status word per device (see
- *    gai4_last_device_status), a static __device__ variable.
+ *    gai4_last_device_status) and the fixed scratch array of
+ *    gai4_qmm_t_noalloc, both static __device__ variables.
  *  - Arguments are validated on the host before anything is launched. A call
  *    that returns anything but GAI4_OK has launched nothing and written nothing.
  *  - Outputs are fully overwritten (no accumulate-into mode).
@@ -145,6 +146,36 @@ size_t gai4_qmm_t_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits, int
 gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group_size,
                             gai4_dtype dtype, int split_k, size_t workspace_bytes,
                             int* path, int* splits);
+
+/*
+ * gai4_qmm_t_noalloc -- gai4_qmm_t for callers that cannot allocate device
+ * memory. (No counterpart on the pages; an addition of this library.)
+ *
+ * Some callers have no device allocator to hand, or must not call one on this
+ * path: a C program that embeds the library without a device-memory manager,
+ * or a latency-critical loop where cudaMalloc's implicit device
+ * synchronization and possible failure are not acceptable. This entry point
+ * takes the same arguments as gai4_qmm_t except the workspace: the split-K
+ * fp32 partials live in a fixed device array inside the library,
+ * GAI4_NOALLOC_SCRATCH_BYTES (8 MiB) long, which every device that loads the
+ * library keeps until the process exits. It allocates nothing, per call or
+ * otherwise.
+ *   - split_k = 0: the split is chosen automatically among those whose
+ *     partials (S * M * N * 4 bytes) fit in the array (no split if none does).
+ *   - split_k = S > 1 whose partials do not fit: GAI4_ERR_WORKSPACE, nothing
+ *     launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on that device.
+ *   - All calls share the array and it keeps the last call's contents; every
+ *     partial a call reads is written earlier by the same call, so nothing
+ *     needs clearing. Calls that overlap on the GPU (different streams, or
+ *     several host threads) race on the array: serialize them.
+ */
+#define GAI4_NOALLOC_SCRATCH_BYTES (8u << 20)
+gai4_status gai4_qmm_t_noalloc(const uint32_t* w_packed, const void* scales, const void* biases,
+                               const void* x, void* out, gai4_dtype dtype, int bits, int group_size,
+                               int64_t M, int64_t N, int64_t K, int split_k, void* stream);
 
 /*
  * gai4_q8_0_gemv -- Q8_0 block-quantized matrix-vector product
