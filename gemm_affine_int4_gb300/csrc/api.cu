@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -93,47 +95,30 @@ static cudaError_t launch_affine(const AffineGemvLaunch& L, int dtype, cudaStrea
 // ---------------------------------------------------------------------------
 static const int64_t kTcMinM = 9;   // tensor-core path from this many x rows up (bf16/f16)
 
-// a split S is legal when every K range is a multiple of 64 and of the group
-// size, and at least 256 long; K < 512 is never split (MLX PR, split-K route)
-static bool split_legal(int64_t K, int gs, int S) {
-    if (S == 1) return true;
-    if (S < 1 || S > 4 || K < 512) return false;
-    const int64_t unit = gs > 64 ? gs : 64;
-    if (K % (S * unit) != 0) return false;
-    return K / S >= 256;
-}
-
-static int auto_split(int64_t M, int64_t N, int64_t K, int gs, size_t ws_bytes, bool tc) {
-    if (!tc) return 1;
-    const int64_t tiles = (N + 127) / 128;
-    const int64_t sms = num_sms();
-    int best = 1;
-    for (int S = 2; S <= 4; ++S) {
-        if (!split_legal(K, gs, S)) continue;
-        if ((size_t)S * (size_t)M * (size_t)N * 4u > ws_bytes) continue;
-        if (tiles * best >= sms) break;   // already fills the GPU
-        best = S;
-    }
-    return best;
-}
-
 static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, int dtype, int split_k,
-                            size_t ws_bytes, bool unlimited_ws, int* path, int* splits) {
+                            size_t ws_bytes, bool unlimited_ws, int* path, SplitPlan* plan) {
     gai4_status st = check_affine_shape(dtype, bits, gs, N, K);
     if (st != GAI4_OK) return st;
     if (M <= 0) return GAI4_ERR_INVALID_ARG;
     if (split_k < 0 || split_k > 4) return GAI4_ERR_UNSUPPORTED;
     const bool tc = dtype != GAI4_F32 && M >= kTcMinM && qmm_tc_supported(M, N, K, bits, gs);
-    int S;
+    SplitPlan p;
     if (split_k == 0) {
-        S = auto_split(M, N, K, gs, unlimited_ws ? (size_t)-1 : ws_bytes, tc);
+        if (tc) {
+            const size_t per_slot = (size_t)M * (size_t)N * sizeof(float);
+            const int max_slots = unlimited_ws ? 4 : (int)std::min<size_t>(4, ws_bytes / per_slot);
+            p = auto_plan(M, N, K, gs, max_slots);
+        } else {
+            uniform_plan(N, K, gs, 1, &p);
+        }
     } else {
-        if (!split_legal(K, gs, split_k)) return GAI4_ERR_UNSUPPORTED;
+        // forced: K cut into split_k equal ranges (multiples of 64 and of the
+        // group size, >= 256 columns; K < 512 is never split)
+        if (!uniform_plan(N, K, gs, split_k, &p)) return GAI4_ERR_UNSUPPORTED;
         if (split_k > 1 && !tc) return GAI4_ERR_UNSUPPORTED;   // only the tensor-core path splits K
-        S = split_k;
     }
     *path = tc ? 1 : 0;
-    *splits = S;
+    *plan = p;
     return GAI4_OK;
 }
 
@@ -195,26 +180,32 @@ gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* b
 
 size_t gai4_qmm_t_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits, int group_size, gai4_dtype dtype,
                                   int split_k) {
-    int path = 0, splits = 1;
-    if (plan_qmm(M, N, K, bits, group_size, dtype, split_k, 0, true, &path, &splits) != GAI4_OK) return 0;
-    return splits > 1 ? (size_t)splits * (size_t)M * (size_t)N * sizeof(float) : 0;
+    int path = 0;
+    SplitPlan plan;
+    if (plan_qmm(M, N, K, bits, group_size, dtype, split_k, 0, true, &path, &plan) != GAI4_OK) return 0;
+    return plan.slots() > 1 ? (size_t)plan.slots() * (size_t)M * (size_t)N * sizeof(float) : 0;
 }
 
 gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group_size, gai4_dtype dtype,
                             int split_k, size_t workspace_bytes, int* path, int* splits) {
     if (!path || !splits) return GAI4_ERR_INVALID_ARG;
-    return plan_qmm(M, N, K, bits, group_size, dtype, split_k, workspace_bytes, false, path, splits);
+    SplitPlan plan;
+    gai4_status st = plan_qmm(M, N, K, bits, group_size, dtype, split_k, workspace_bytes, false, path, &plan);
+    if (st == GAI4_OK) *splits = plan.slots();
+    return st;
 }
 
 gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void* biases, const void* x, void* out,
                        gai4_dtype dtype, int bits, int group_size, int64_t M, int64_t N, int64_t K, int split_k,
                        void* workspace, size_t workspace_bytes, void* stream) {
-    int path = 0, splits = 1;
+    int path = 0;
+    SplitPlan plan;
     gai4_status st = plan_qmm(M, N, K, bits, group_size, dtype, split_k, workspace ? workspace_bytes : 0, false,
-                              &path, &splits);
+                              &path, &plan);
     if (st != GAI4_OK) return st;
     if (!w_packed || !scales || !biases || !x || !out) return GAI4_ERR_INVALID_ARG;
     if (!aligned16(w_packed) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    const int splits = plan.slots();
     if (splits > 1) {
         if (!workspace || workspace_bytes < (size_t)splits * (size_t)M * (size_t)N * sizeof(float))
             return GAI4_ERR_WORKSPACE;
@@ -237,14 +228,14 @@ gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void*
     T.K = K;
     T.bits = bits;
     T.group_size = group_size;
-    T.splits = splits;
+    T.plan = plan;
     T.is_bf16 = dtype == GAI4_BF16;
     T.status = status_ptr();
     T.spin_limit = 2000000000LL;   // ~1 s of SM clock per wait
     if (!T.status) return GAI4_ERR_CUDA;
     cudaError_t e = launch_qmm_tc(T, s);
     if (e != cudaSuccess) return GAI4_ERR_CUDA;
-    if (splits > 1) e = launch_splitk_reduce(T.partials, out, M, N, splits, dtype, s);
+    if (splits > 1) e = launch_splitk_reduce(T.partials, out, M, N, plan, dtype, s);
     return from_cuda(e);
 }
 

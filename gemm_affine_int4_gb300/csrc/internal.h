@@ -26,6 +26,26 @@ cudaError_t launch_affine_gemv_bf16(const AffineGemvLaunch& L, cudaStream_t s);
 cudaError_t launch_affine_gemv_f16(const AffineGemvLaunch& L, cudaStream_t s);
 cudaError_t launch_affine_gemv_f32(const AffineGemvLaunch& L, cudaStream_t s);
 
+// K-split plan of the tensor-core qmm_t. The N axis is cut into 128-row
+// tiles; tile t is cut along K into s_t pieces (s_t = s_base + 1 for the first
+// n_extra tiles, s_base for the rest), piece j of s_t covering K columns
+// [(j*KU/s_t)*unit, ((j+1)*KU/s_t)*unit), KU = K/unit. Piece j of every tile
+// writes fp32 partial slot j. A uniform split S is {S, 0}.
+struct SplitPlan {
+    int tiles;
+    int s_base;
+    int n_extra;
+    int unit;        // K granularity of the cuts: max(64, group_size)
+    __host__ __device__ int slots() const { return s_base + (n_extra > 0 ? 1 : 0); }
+    __host__ __device__ int64_t pieces() const { return (int64_t)n_extra * (s_base + 1) + (int64_t)(tiles - n_extra) * s_base; }
+};
+// piece counts per tile legal for K (pieces >= 256 columns; K < 512 unsplit), at most 4
+int max_pieces(int64_t K, int unit);
+// uniform split S (1..4) if legal
+bool uniform_plan(int64_t N, int64_t K, int gs, int S, SplitPlan* out);
+// balanced automatic plan for the device's SM count, limited to max_slots partial slots
+SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots);
+
 // tensor-core qmm_t (qmm_tc.cu)
 struct QmmTcLaunch {
     const uint32_t* w;
@@ -33,10 +53,10 @@ struct QmmTcLaunch {
     const void* biases;
     const void* x;      // [M, K] bf16/f16
     void* out;          // [M, N]
-    float* partials;    // [S, M, N] fp32 when splits > 1
+    float* partials;    // [slots, M, N] fp32 when plan.slots() > 1
     int64_t M, N, K;
     int bits, group_size;
-    int splits;
+    SplitPlan plan;
     int is_bf16;
     int* status;        // device status word
     long long spin_limit;
@@ -53,9 +73,10 @@ cudaError_t launch_dequantize(const uint32_t* packed, const void* scales, const 
                               float* out, int dtype, int bits, int gs, int64_t N, int64_t K,
                               cudaStream_t s);
 
-// split-K reduce (qmm_tc.cu): out[m, n] = T(sum_s partials[s, m, n])
+// split-K reduce (qmm_tc.cu): out[m, n] = T(sum_{j < s_t} partials[j, m, n]),
+// s_t the piece count of n's tile
 cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N,
-                                 int splits, int dtype, cudaStream_t s);
+                                 const SplitPlan& plan, int dtype, cudaStream_t s);
 
 // block-quantized GEMVs (blockq.cu)
 cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N,

@@ -34,6 +34,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,48 +46,98 @@ namespace gai4 {
 // rounded once (MLX PR, Correctness: fp32 partials, one rounding after the sum)
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void splitk_reduce_kernel(const float* __restrict__ P, typename T::storage* __restrict__ out,
-                                     int64_t MN, int S) {
-    const int64_t i4 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (i4 >= MN) return;
-    if (i4 + 4 <= MN && (MN & 3) == 0) {
-        float4 acc = *reinterpret_cast<const float4*>(P + i4);
-        for (int s = 1; s < S; ++s) {
-            const float4 v = *reinterpret_cast<const float4*>(P + (int64_t)s * MN + i4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        out[i4 + 0] = T::from_f32(acc.x);
-        out[i4 + 1] = T::from_f32(acc.y);
-        out[i4 + 2] = T::from_f32(acc.z);
-        out[i4 + 3] = T::from_f32(acc.w);
-    } else {
-        for (int64_t i = i4; i < i4 + 4 && i < MN; ++i) {
-            float acc = P[i];
-            for (int s = 1; s < S; ++s) acc += P[(int64_t)s * MN + i];
-            out[i] = T::from_f32(acc);
-        }
-    }
+__global__ void splitk_reduce_kernel(const float* __restrict__ P, typename T::storage* __restrict__ out, int64_t M,
+                                     int64_t N, SplitPlan plan) {
+    const int64_t MN = M * N;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= MN) return;
+    const int64_t n = i % N;
+    const int tile = (int)(n / 128);
+    const int s_t = plan.s_base + (tile < plan.n_extra ? 1 : 0);
+    float acc = P[i];
+    for (int s = 1; s < s_t; ++s) acc += P[(int64_t)s * MN + i];
+    out[i] = T::from_f32(acc);
 }
 
-cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N, int splits, int dtype,
-                                 cudaStream_t s) {
+cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
+                                 int dtype, cudaStream_t s) {
     const int64_t MN = M * N;
-    const unsigned blocks = (unsigned)(((MN + 3) / 4 + 255) / 256);
+    const unsigned blocks = (unsigned)((MN + 255) / 256);
     switch (dtype) {
     case GAI4_F16:
-        splitk_reduce_kernel<F16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), MN, splits);
+        splitk_reduce_kernel<F16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), M, N, plan);
         break;
     case GAI4_F32:
-        splitk_reduce_kernel<F32><<<blocks, 256, 0, s>>>(partials, static_cast<float*>(out), MN, splits);
+        splitk_reduce_kernel<F32><<<blocks, 256, 0, s>>>(partials, static_cast<float*>(out), M, N, plan);
         break;
     default:
-        splitk_reduce_kernel<BF16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), MN, splits);
+        splitk_reduce_kernel<BF16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), M, N, plan);
         break;
     }
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// K-split planning (MLX PR: at most 4 pieces of >= 256 columns, K < 512 not
+// split). Pieces of one tile may differ in length by one unit, so that the
+// number of CTAs can match the number of SMs instead of spilling into a
+// second, mostly idle wave.
+// ---------------------------------------------------------------------------
+int max_pieces(int64_t K, int unit) {
+    if (K < 512) return 1;
+    const int64_t KU = K / unit;
+    int best = 1;
+    for (int S = 2; S <= 4; ++S)
+        if ((KU / S) * unit >= 256) best = S;
+    return best;
+}
+
+bool uniform_plan(int64_t N, int64_t K, int gs, int S, SplitPlan* out) {
+    SplitPlan p;
+    p.tiles = (int)((N + 127) / 128);
+    p.unit = gs > 64 ? gs : 64;
+    p.n_extra = 0;
+    p.s_base = S;
+    if (S < 1 || S > 4 || K % p.unit != 0) return false;
+    if (S > 1 && (K < 512 || K % ((int64_t)S * p.unit) != 0 || K / S < 256)) return false;
+    *out = p;
+    return true;
+}
+
+SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
+    SplitPlan p;
+    p.tiles = (int)((N + 127) / 128);
+    p.unit = gs > 64 ? gs : 64;
+    p.s_base = 1;
+    p.n_extra = 0;
+    const int cap = std::min(max_pieces(K, p.unit), std::max(1, max_slots));
+    const int64_t mchunks = (M + 255) / 256;
+    const int64_t avail = std::max<int64_t>(1, num_sms() / mchunks);   // CTAs per M chunk in one wave
+    const int64_t KU = K / p.unit;
+    const int64_t T = p.tiles;
+    // candidate 1: uniform S in waves
+    int64_t best_cost = -1;
+    for (int S = 1; S <= cap; ++S) {
+        const int64_t waves = (T * S + avail - 1) / avail;
+        const int64_t cost = waves * ((KU + S - 1) / S);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            p.s_base = S;
+            p.n_extra = 0;
+        }
+    }
+    // candidate 2: one wave with s_base or s_base + 1 pieces per tile
+    if (T <= avail) {
+        const int sb = (int)std::min<int64_t>(cap, avail / T);
+        const int ne = sb < cap ? (int)std::min<int64_t>(T, avail - T * sb) : 0;
+        const int64_t cost = (KU + sb - 1) / sb;
+        if (cost < best_cost) {
+            best_cost = cost;
+            p.s_base = sb;
+            p.n_extra = ne;
+        }
+    }
+    return p;
 }
 
 // ---------------------------------------------------------------------------
@@ -94,14 +146,16 @@ cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, in
 namespace tc {
 
 constexpr int kTileN = 128;      // weight rows per CTA (MMA M)
-constexpr int kBK = 128;         // K columns per pipeline stage
-constexpr int kMaxWStages = 12;  // packed-weight ring (runtime depth <= this)
-constexpr int kAStages = 2;      // tensor-memory A ring (64 columns each)
+constexpr int kBK = 256;         // K columns per weight / A stage
+constexpr int kXBK = 128;        // K columns per activation stage (two 64-column swizzle atoms)
+constexpr int kMaxWStages = 8;   // packed-weight ring (runtime depth <= this)
+constexpr int kMaxAStages = 3;   // tensor-memory A ring (128 columns each; runtime depth <= this)
+constexpr int kMaxXStages = 6;   // activation ring (runtime depth <= this)
 constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
-// 12 warps: a multiple of 4, so that warp w of every co-resident CTA runs on
-// SM sub-partition w % 4 and reaches tensor-memory lanes 32 (w % 4) .. +31
-constexpr int kThreads = 32 * 12;
+constexpr int kTmemCols = 512;   // one CTA per SM owns all of tensor memory
+constexpr int kDequantWarps = 8;    // 2 per tensor-memory lane quadrant, 128 columns each
 constexpr int kDequantWarp0 = 4;
+constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -162,15 +216,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     return true;
 }
 
-// warp-uniform wait: lane 0 spins, the warp then reconverges (the following
-// tcgen05 .sync.aligned instructions need every lane, converged) and takes
-// lane 0's answer
+// warp-uniform wait: every lane observes the phase itself (each lane's own
+// acquire makes the asynchronously written data visible to it), then the warp
+// reconverges (the following tcgen05 .sync.aligned instructions need every
+// lane, converged) and agrees on the outcome
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
-    const int lane = threadIdx.x & 31;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, c) ? 1 : 0;
+    const bool ok = mbar_wait(bar, parity, c);
     __syncwarp();
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
@@ -225,6 +278,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
@@ -258,20 +320,38 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
 struct Params {
     const uint16_t* scales;
     const uint16_t* biases;
-    void* out;            // [M, N] T (splits == 1)
-    float* partials;      // [S, M, N] fp32 (splits > 1)
+    void* out;            // [M, N] T (one piece per tile)
+    float* partials;      // [slots, M, N] fp32 (several pieces)
     int64_t M, N, K;
     int64_t groups;       // K / group_size
     int gs_log2;          // log2(group_size)
-    int k_per_split;      // K columns per split (multiple of 64)
-    int splits;
+    SplitPlan plan;
     int mt;               // MMA N: x rows of this CTA rounded up to 16 (<= 256)
     int x_stages;
     int w_stages;
-    int tmem_cols;        // allocated columns (power of two)
+    int a_stages;
     int* status;
     long long spin_limit;
 };
+
+// piece blockIdx.x of the plan -> tile, piece index, K range
+__device__ __forceinline__ void piece_of(const SplitPlan& pl, int64_t K, int p, int& tile, int& j, int& s_t,
+                                         int64_t& k0, int64_t& k1) {
+    const int big = pl.n_extra * (pl.s_base + 1);
+    if (p < big) {
+        tile = p / (pl.s_base + 1);
+        j = p - tile * (pl.s_base + 1);
+        s_t = pl.s_base + 1;
+    } else {
+        const int q = p - big;
+        tile = pl.n_extra + q / pl.s_base;
+        j = q - (tile - pl.n_extra) * pl.s_base;
+        s_t = pl.s_base;
+    }
+    const int64_t KU = K / pl.unit;
+    k0 = (j * KU / s_t) * pl.unit;
+    k1 = ((j + 1) * KU / s_t) * pl.unit;
+}
 
 // ---------------------------------------------------------------------------
 // 4-bit codes: one 32-bit word (8 codes, low nibble first) -> 4 registers of
@@ -302,42 +382,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int mt = p.mt;
-    const int XS = p.x_stages;
-    const int kWStages = p.w_stages;
-    const uint32_t x_stage_bytes = (uint32_t)mt * kBK * 2;     // two 64-column swizzle atoms
-    const uint32_t w_stage_bytes = kTileN * kBK / 2;           // 4-bit codes
-    uint8_t* xbuf = smem;                                      // XS x stages
-    uint8_t* wbuf = xbuf + (size_t)XS * x_stage_bytes;         // kWStages w stages
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + (size_t)kWStages * w_stage_bytes);
+    const int XS = p.x_stages, WS = p.w_stages, AS = p.a_stages;
+    const uint32_t x_stage_bytes = (uint32_t)mt * kXBK * 2;    // two 64-column swizzle atoms
+    const uint32_t w_stage_bytes = kTileN * kBK / 2;           // 4-bit codes, 128-byte rows
+    uint8_t* xbuf = smem;
+    uint8_t* wbuf = xbuf + (size_t)XS * x_stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + (size_t)WS * w_stage_bytes);
     uint64_t* w_full = bars;
     uint64_t* w_empty = w_full + kMaxWStages;
     uint64_t* x_full = w_empty + kMaxWStages;
-    uint64_t* x_empty = x_full + 4;
-    uint64_t* a_full = x_empty + 4;
-    uint64_t* a_empty = a_full + kAStages;
-    uint64_t* acc_full = a_empty + kAStages;
+    uint64_t* x_empty = x_full + kMaxXStages;
+    uint64_t* a_full = x_empty + kMaxXStages;
+    uint64_t* a_empty = a_full + kMaxAStages;
+    uint64_t* acc_full = a_empty + kMaxAStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n0 = (int64_t)blockIdx.x * kTileN;
-    const int split = blockIdx.y;
+    int tile, piece, s_t;
+    int64_t k_begin, k_end;
+    piece_of(p.plan, p.K, blockIdx.x, tile, piece, s_t, k_begin, k_end);
+    const int64_t n0 = (int64_t)tile * kTileN;
     const int64_t m0 = (int64_t)blockIdx.z * kMaxMt;
-    const int64_t k_begin = (int64_t)split * p.k_per_split;
-    const int nk64 = p.k_per_split / 64;                       // 64-column halves in this split
-    const int nst = (nk64 + 1) / 2;                            // 128-column stages
+    const int nk64 = (int)((k_end - k_begin) / 64);            // 64-column units in this piece
+    const int nst = (nk64 + 3) / 4;                            // 256-column weight / A stages
+    const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kWStages; ++i) {
+        for (int i = 0; i < WS; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], 8);          // one arrive per dequant warp
+            mbar_init(&w_empty[i], kDequantWarps);   // one arrive per dequantize warp
         }
         for (int i = 0; i < XS; ++i) {
             mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 1);          // tcgen05.commit
+            mbar_init(&x_empty[i], 1);               // tcgen05.commit
         }
-        for (int i = 0; i < kAStages; ++i) {
-            mbar_init(&a_full[i], 8);
+        for (int i = 0; i < AS; ++i) {
+            mbar_init(&a_full[i], kDequantWarps);
             mbar_init(&a_empty[i], 1);
         }
         mbar_init(acc_full, 1);
@@ -347,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {   // tensor-memory allocation (whole warp)
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(p.tmem_cols)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -355,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t acc_col = 0;                  // accumulator: columns [0, mt)
-    const uint32_t a_col0 = (uint32_t)p.tmem_cols - 64u * kAStages;   // A ring at the top
+    const uint32_t acc_col = 0;                                      // accumulator: columns [0, mt)
+    const uint32_t a_col0 = (uint32_t)kTmemCols - 128u * (uint32_t)AS;   // A ring at the top
     Ctl ctl{p.status, p.spin_limit, abort_flag};
 
     if (warp == 0) {
@@ -364,132 +445,170 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
-                const int s = i % kWStages;
-                if (!mbar_wait(&w_empty[s], ((i / kWStages) & 1) ^ 1, ctl)) break;
+                const int s = i % WS;
+                if (!mbar_wait(&w_empty[s], ((i / WS) & 1) ^ 1, ctl)) break;
                 mbar_arrive_expect_tx(&w_full[s], w_stage_bytes);
-                // x coordinate in 32-bit words: (k_begin + 128 i) * 4 / 32
+                // x coordinate in 32-bit words: (k_begin + 256 i) * 4 / 32
                 tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)((k_begin + kBK * i) / 8),
                             (int)n0);
                 ++issued;
             }
             // drain: every issued copy has landed before the CTA may exit
-            for (int i = (issued > kWStages ? issued - kWStages : 0); i < issued; ++i)
-                mbar_wait_drain(&w_full[i % kWStages], (i / kWStages) & 1, p.spin_limit, p.status);
+            for (int i = (issued > WS ? issued - WS : 0); i < issued; ++i)
+                mbar_wait_drain(&w_full[i % WS], (i / WS) & 1, p.spin_limit, p.status);
         }
     } else if (warp == 1) {
         // ---------------- activation producer ----------------
         if (lane == 0) {
             int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % XS;
-                if (!mbar_wait(&x_empty[s], ((i / XS) & 1) ^ 1, ctl)) break;
+            for (int j = 0; j < nxs; ++j) {
+                const int s = j % XS;
+                if (!mbar_wait(&x_empty[s], ((j / XS) & 1) ^ 1, ctl)) break;
                 mbar_arrive_expect_tx(&x_full[s], x_stage_bytes);
                 uint8_t* dst = xbuf + (size_t)s * x_stage_bytes;
-                const int kx = (int)(k_begin + kBK * i);
+                const int kx = (int)(k_begin + kXBK * j);
                 tma_load_2d(dst, &xmap, &x_full[s], kx, (int)m0);
                 tma_load_2d(dst + (size_t)mt * 128, &xmap, &x_full[s], kx + 64, (int)m0);
                 ++issued;
             }
-            for (int i = (issued > XS ? issued - XS : 0); i < issued; ++i)
-                mbar_wait_drain(&x_full[i % XS], (i / XS) & 1, p.spin_limit, p.status);
+            for (int j = (issued > XS ? issued - XS : 0); j < issued; ++j)
+                mbar_wait_drain(&x_full[j % XS], (j / XS) & 1, p.spin_limit, p.status);
         }
     } else if (warp == 2) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = make_idesc(BF ? 1 : 0, mt);
             uint32_t acc_flag = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int sa = i % kAStages, sx = i % XS;
-                if (!mbar_wait(&a_full[sa], (i / kAStages) & 1, ctl)) break;
-                if (!mbar_wait(&x_full[sx], (i / XS) & 1, ctl)) break;
-                fence_after();
-                const int kk_end = (2 * i + 1 < nk64) ? 8 : 4;   // last stage may hold one 64-column half
-                const uint32_t xaddr = smem_u32(xbuf + (size_t)sx * x_stage_bytes);
-                for (int kk = 0; kk < kk_end; ++kk) {
-                    const uint32_t a_t = tmem_base + a_col0 + (uint32_t)sa * 64u + (uint32_t)kk * 8u;
-                    const uint32_t baddr = xaddr + (uint32_t)(kk >> 2) * (uint32_t)mt * 128u + (uint32_t)(kk & 3) * 32u;
-                    mma_f16_tmem_a(tmem_base + acc_col, a_t, sw128_desc(baddr), idesc, acc_flag);
-                    acc_flag = 1;
+            bool ok = true;
+            for (int i = 0; i < nst && ok; ++i) {
+                const int sa = i % AS;
+                if (!mbar_wait(&a_full[sa], (i / AS) & 1, ctl)) break;
+                for (int hh = 0; hh < 2; ++hh) {        // the two activation stages of this A stage
+                    const int j = 2 * i + hh;
+                    if (j >= nxs) break;
+                    const int sx = j % XS;
+                    if (!mbar_wait(&x_full[sx], (j / XS) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const int kk_end = (2 * j + 1 < nk64) ? 8 : 4;   // a stage may end with one 64-column unit
+                    const uint32_t xaddr = smem_u32(xbuf + (size_t)sx * x_stage_bytes);
+                    for (int kk = 0; kk < kk_end; ++kk) {
+                        const uint32_t a_t =
+                            tmem_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)hh * 64u + (uint32_t)kk * 8u;
+                        const uint32_t baddr =
+                            xaddr + (uint32_t)(kk >> 2) * (uint32_t)mt * 128u + (uint32_t)(kk & 3) * 32u;
+                        mma_f16_tmem_a(tmem_base + acc_col, a_t, sw128_desc(baddr), idesc, acc_flag);
+                        acc_flag = 1;
+                    }
+                    mma_commit(&x_empty[sx]);
                 }
+                if (!ok) break;
                 mma_commit(&a_empty[sa]);
-                mma_commit(&x_empty[sx]);
             }
             mma_commit(acc_full);   // completes when every MMA above has finished
             // no MMA may still run when tensor memory is freed
             mbar_wait_drain(acc_full, 0, p.spin_limit, p.status);
         }
     } else if (warp == 3) {
-        // idle
+        // idle (keeps the role warps a multiple of 4)
     } else {
         // ---------------- dequantize, then epilogue ----------------
         const int dw = warp - kDequantWarp0;        // 0..7
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
-        const int half = dw >> 2;                   // which 64 of the stage's 128 columns
+        const int half = dw >> 2;                   // which 128 of the stage's 256 columns
         const int r = quad * 32 + lane;             // weight row within the tile
         const int64_t row = n0 + r;
         const bool row_ok = row < p.N;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint16_t* srow = p.scales + row * p.groups;
+        const uint16_t* brow = p.biases + row * p.groups;
+        const uint8_t* wrow = wbuf + (size_t)r * 128;
+
+        // scale / bias of the four 32-column quarters of this thread's 128
+        // columns (a quarter lies in one group), loaded two stages before use
+        auto load_sb = [&](int i, uint32_t (&sv)[4], uint32_t (&bv)[4]) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sv[q] = 0u;
+                bv[q] = 0u;
+                const int unit = 4 * i + 2 * half + (q >> 1);   // 64-column unit of this quarter
+                if (i < nst && unit < nk64 && row_ok) {
+                    const int64_t g = (k_begin + (int64_t)kBK * i + 128 * half + 32 * q) >> p.gs_log2;
+                    sv[q] = __ldg(srow + g);
+                    bv[q] = __ldg(brow + g);
+                }
+            }
+        };
+        uint32_t s0[4], b0[4], s1[4], b1[4];
+        load_sb(0, s0, b0);
+        load_sb(1, s1, b1);
 
         for (int i = 0; i < nst; ++i) {
-            const int sw = i % kWStages, sa = i % kAStages;
-            const bool active = (2 * i + half) < nk64;   // this half exists in the split
-            if (!warp_wait(&w_full[sw], (i / kWStages) & 1, ctl)) break;
-            // the row's 32 bytes of this half: 64-byte rows, 64-byte TMA swizzle
-            // (16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3))
-            uint32_t wv[8];
-            {
-                const uint8_t* rowp = wbuf + (size_t)sw * w_stage_bytes + (size_t)r * 64;
-                const int sx = (r >> 1) & 3;
-                const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * half) ^ sx));
-                const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * half + 1) ^ sx));
-                wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
-                wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+            const int sw = i % WS, sa = i % AS;
+            uint32_t sc[4], bc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sc[q] = s0[q];
+                bc[q] = b0[q];
+                s0[q] = s1[q];
+                b0[q] = b1[q];
             }
+            load_sb(i + 2, s1, b1);
+            if (!warp_wait(&w_full[sw], (i / WS) & 1, ctl)) break;
+            // this thread's 64 bytes (128 codes) of the row: 128-byte rows,
+            // 128-byte TMA swizzle (16-byte chunk c of row r at chunk c ^ (r & 7))
+            uint4 v[4];
+            const uint8_t* rowp = wrow + (size_t)sw * w_stage_bytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                v[c] = *reinterpret_cast<const uint4*>(rowp + 16 * ((4 * half + c) ^ (r & 7)));
+            // the stage is refilled by TMA (async proxy): order these generic
+            // reads before that write, then release the stage
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[sw]);
 
-            uint32_t o[32];
-            if (active) {
-                // scale / bias of the (one or two) groups of these 64 columns
-                const int64_t k0 = k_begin + (int64_t)kBK * i + 64 * half;
-                const int64_t g0 = k0 >> p.gs_log2;
-                const int64_t g1 = (k0 + 32) >> p.gs_log2;
-                uint32_t s2a = 0, b2a = 0, s2b = 0, b2b = 0;
-                if (row_ok) {
-                    const uint32_t sa_ = __ldg(p.scales + row * p.groups + g0);
-                    const uint32_t ba_ = __ldg(p.biases + row * p.groups + g0);
-                    const uint32_t sb_ = __ldg(p.scales + row * p.groups + g1);
-                    const uint32_t bb_ = __ldg(p.biases + row * p.groups + g1);
-                    s2a = sa_ | (sa_ << 16);
-                    b2a = ba_ | (ba_ << 16);
-                    s2b = sb_ | (sb_ << 16);
-                    b2b = bb_ | (bb_ << 16);
-                }
-#pragma unroll
-                for (int wi = 0; wi < 8; ++wi) {
-                    if (wi < 4) dequant_word4<BF>(wv[wi], s2a, b2a, &o[4 * wi]);
-                    else dequant_word4<BF>(wv[wi], s2b, b2b, &o[4 * wi]);
-                }
-            }
-            if (!warp_wait(&a_empty[sa], ((i / kAStages) & 1) ^ 1, ctl)) break;
+            if (!warp_wait(&a_empty[sa], ((i / AS) & 1) ^ 1, ctl)) break;
             fence_after();
-            if (active) {
-                tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 64u + (uint32_t)half * 32u, o);
-                tmem_st_wait();
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {    // two 64-column units -> 32 TMEM columns each
+                const int unit = 4 * i + 2 * half + sub;
+                if (unit < nk64) {
+                    uint32_t o[32];
+                    const uint32_t s2a = sc[2 * sub] | (sc[2 * sub] << 16), b2a = bc[2 * sub] | (bc[2 * sub] << 16);
+                    const uint32_t s2b = sc[2 * sub + 1] | (sc[2 * sub + 1] << 16);
+                    const uint32_t b2b = bc[2 * sub + 1] | (bc[2 * sub + 1] << 16);
+                    const uint4 va = v[2 * sub], vb = v[2 * sub + 1];
+                    dequant_word4<BF>(va.x, s2a, b2a, &o[0]);
+                    dequant_word4<BF>(va.y, s2a, b2a, &o[4]);
+                    dequant_word4<BF>(va.z, s2a, b2a, &o[8]);
+                    dequant_word4<BF>(va.w, s2a, b2a, &o[12]);
+                    dequant_word4<BF>(vb.x, s2b, b2b, &o[16]);
+                    dequant_word4<BF>(vb.y, s2b, b2b, &o[20]);
+                    dequant_word4<BF>(vb.z, s2b, b2b, &o[24]);
+                    dequant_word4<BF>(vb.w, s2b, b2b, &o[28]);
+                    tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)half * 64u +
+                                  (uint32_t)sub * 32u,
+                              o);
+                }
             }
+            tmem_st_wait();
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[sa]);
         }
 
-        // epilogue: accumulator rows -> fp32 partials or T output
+        // epilogue: accumulator rows -> fp32 partials or T output; the 2 warps
+        // of a quadrant take 8-column chunks alternately
         const bool ok = warp_wait(acc_full, 0, ctl);
         fence_after();
         if (ok) {
             const int64_t mrows = min((int64_t)mt, p.M - m0);
-            const int cols_half = mt / 2;              // multiple of 8
-            const int c_begin = half * cols_half;
-            for (int c = c_begin; c < c_begin + cols_half; c += 8) {
+            const bool split = p.plan.slots() > 1;
+            float* pslot = p.partials + (int64_t)piece * p.M * p.N;
+            for (int c = 8 * half; c < mt; c += 16) {
                 uint32_t v[8];
                 __syncwarp();
                 tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)c, v);
@@ -501,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (m < mrows) {
                             const float f = __uint_as_float(v[j]);
                             const int64_t idx = (m0 + m) * p.N + row;
-                            if (p.splits > 1) {
-                                p.partials[(int64_t)split * p.M * p.N + idx] = f;
+                            if (split) {
+                                pslot[idx] = f;
                             } else if (BF) {
                                 static_cast<uint16_t*>(p.out)[idx] = BF16::from_f32(f);
                             } else {
@@ -520,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         __syncwarp();
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -530,12 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using tc::kAStages;
 using tc::kBK;
+using tc::kMaxAStages;
 using tc::kMaxMt;
+using tc::kMaxWStages;
+using tc::kMaxXStages;
 using tc::kThreads;
 using tc::kTileN;
-using tc::kMaxWStages;
+using tc::kTmemCols;
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -560,32 +681,23 @@ int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int gs) {
     return 1;
 }
 
-static int pow2_at_least(int v) {
-    int p = 32;
-    while (p < v) p <<= 1;
-    return p;
-}
-
 cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int64_t M = L.M, N = L.N, K = L.K;
-    const int S = L.splits;
-    const int64_t kps = K / S;
     const int64_t mchunks = (M + kMaxMt - 1) / kMaxMt;
     const int64_t mrows = M < kMaxMt ? M : kMaxMt;
     const int mt = (int)((mrows + 15) / 16 * 16);
-    const int xs = mt > 128 ? 2 : 3;
 
-    // packed weights: u32 [N, K/8], box {16 words = 128 columns, 128 rows}, 64-byte swizzle
+    // packed weights: u32 [N, K/8], box {32 words = 256 columns, 128 rows}, 128-byte swizzle
     CUtensorMap wmap, xmap;
     {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {16, 128};
+        cuuint32_t box[2] = {32, 128};
         cuuint32_t es[2] = {1, 1};
         if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(L.w), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
@@ -600,20 +712,25 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // One CTA per SM: a second co-resident CTA of this kernel would run warps
-    // whose tensor-memory lane quadrant differs from (warp index % 4), which
-    // the dequantize and epilogue roles rely on. The shared memory request is
-    // therefore kept above half of the SM's capacity; the space goes to a
-    // deeper packed-weight ring.
+
+    // Ring depths. One CTA per SM: a second co-resident CTA of this kernel
+    // could run warps whose tensor-memory lane quadrant differs from
+    // (warp index % 4), which the dequantize and epilogue roles rely on; the
+    // kernel also takes all 512 tensor-memory columns. The shared-memory
+    // request is kept above half of the SM's capacity.
+    const int xs = mt > 128 ? 2 : (mt > 64 ? 4 : kMaxXStages);
+    int as = (kTmemCols - mt) / 128;
+    as = as > kMaxAStages ? kMaxAStages : as;
     const size_t kBars = 512;
-    const size_t x_bytes = (size_t)xs * mt * kBK * 2;
+    const size_t x_bytes = (size_t)xs * mt * tc::kXBK * 2;
     const size_t w_stage = (size_t)kTileN * kBK / 2;
-    const size_t budget = 200 * 1024;
+    const size_t budget = 210 * 1024;
     int ws = (int)((budget - 1024 - kBars - x_bytes) / w_stage);
-    ws = ws < 4 ? 4 : (ws > kMaxWStages ? kMaxWStages : ws);
+    ws = ws < 3 ? 3 : (ws > kMaxWStages ? kMaxWStages : ws);
     size_t smem = 1024 + x_bytes + (size_t)ws * w_stage + kBars;
     if (smem < 120 * 1024) smem = 120 * 1024;
-    static_assert((2 * kMaxWStages + 2 * 4 + 2 * 2 + 1) * 8 + 8 <= 512, "barrier area");
+    static_assert((2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxAStages + 1) * 8 + 8 <= 512, "barrier area");
+
     tc::Params p;
     p.scales = static_cast<const uint16_t*>(L.scales);
     p.biases = static_cast<const uint16_t*>(L.biases);
@@ -626,15 +743,13 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     int lg = 0;
     while ((1 << lg) < L.group_size) ++lg;
     p.gs_log2 = lg;
-    p.k_per_split = (int)kps;
-    p.splits = S;
+    p.plan = L.plan;
     p.mt = mt;
     p.x_stages = xs;
     p.w_stages = ws;
-    p.tmem_cols = pow2_at_least(mt + 64 * kAStages);
+    p.a_stages = as;
     p.status = L.status;
     p.spin_limit = L.spin_limit;
-
 
     auto kern = L.is_bf16 ? tc::qmm_tc4_kernel<true> : tc::qmm_tc4_kernel<false>;
     static unsigned long long configured[2] = {0ull, 0ull};
@@ -646,7 +761,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[which] |= 1ull << dev;
     }
-    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)S, (unsigned)mchunks);
+    dim3 grid((unsigned)L.plan.pieces(), 1u, (unsigned)mchunks);
     kern<<<grid, kThreads, smem, stream>>>(wmap, xmap, p);
     return cudaGetLastError();
 }
