@@ -17,9 +17,13 @@
 //   warp 0      TMA producer of the packed-weight tiles (ring of kWStages)
 //   warp 1      TMA producer of the activation tiles (ring of kXStages),
 //               128-byte swizzled = the canonical K-major UMMA layout
-//   warp 2      MMA issuer (one thread): tcgen05.mma kind::f16, A operand
-//               from tensor memory, B operand (activations) from shared memory
-//   warp 3      idle (keeps the warp count a multiple of 4)
+//   warps 2-3   MMA issuers: tcgen05.mma kind::f16, A operand from tensor
+//               memory, B operand (activations) from shared memory. The whole
+//               warp runs the issue loop (warp-uniform control flow) and
+//               elect.sync picks the lane that issues: a converged warp issues
+//               MMAs about twice as fast as one divergent lane. With two
+//               issuers, issuer j takes the stages i = j (mod 2) into its own
+//               accumulator, and the epilogue adds the two in a fixed order.
 //   warps 4-11  dequantize: thread t of warp quadrant q owns weight row
 //               32q + t and half of the stage's 128 K columns; it decodes the
 //               codes, computes w_hat = fma(q, s, b) in bf16x2/f16x2 (one
@@ -153,6 +157,7 @@ constexpr int kMaxAStages = 3;   // tensor-memory A ring (128 columns each; runt
 constexpr int kMaxXStages = 6;   // activation ring (runtime depth <= this)
 constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
 constexpr int kTmemCols = 512;   // one CTA per SM owns all of tensor memory
+constexpr int kMaxIssuers = 2;   // MMA issuer warps (2 and 3), one accumulator each
 constexpr int kDequantWarps = 8;    // 2 per tensor-memory lane quadrant, 128 columns each
 constexpr int kDequantWarp0 = 4;
 constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
@@ -267,6 +272,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// the same two operations executed by a converged warp: one elected lane issues
+__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 // 32 consecutive 32-bit columns of this thread's TMEM lane
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -330,6 +351,7 @@ struct Params {
     int x_stages;
     int w_stages;
     int a_stages;
+    int n_issuers;        // MMA issuer warps = accumulators (1 or 2)
     int* status;
     long long spin_limit;
 };
@@ -421,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_full[i], kDequantWarps);
             mbar_init(&a_empty[i], 1);
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, p.n_issuers);         // one commit per issuer
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -436,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t acc_col = 0;                                      // accumulator: columns [0, mt)
+    const uint32_t acc_col = 0;   // accumulator of issuer j: columns [j * mt, (j + 1) * mt)
+    const int NI = p.n_issuers;
     const uint32_t a_col0 = (uint32_t)kTmemCols - 128u * (uint32_t)AS;   // A ring at the top
     Ctl ctl{p.status, p.spin_limit, abort_flag};
 
@@ -474,45 +497,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = (issued > XS ? issued - XS : 0); j < issued; ++j)
                 mbar_wait_drain(&x_full[j % XS], (j / XS) & 1, p.spin_limit, p.status);
         }
-    } else if (warp == 2) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+    } else if (warp == 2 || warp == 3) {
+        // ---------------- MMA issuers (whole warps) ----------------
+        const int jw = warp - 2;
+        if (jw < NI) {
             const uint32_t idesc = make_idesc(BF ? 1 : 0, mt);
+            const uint32_t acc_tm = tmem_base + acc_col + (uint32_t)(jw * mt);
             uint32_t acc_flag = 0;
-            bool ok = true;
-            for (int i = 0; i < nst && ok; ++i) {
+            for (int i = jw; i < nst; i += NI) {
                 const int sa = i % AS;
-                if (!mbar_wait(&a_full[sa], (i / AS) & 1, ctl)) break;
+                if (!warp_wait(&a_full[sa], (i / AS) & 1, ctl)) break;
+                bool ok = true;
                 for (int hh = 0; hh < 2; ++hh) {        // the two activation stages of this A stage
                     const int j = 2 * i + hh;
                     if (j >= nxs) break;
                     const int sx = j % XS;
-                    if (!mbar_wait(&x_full[sx], (j / XS) & 1, ctl)) {
+                    if (!warp_wait(&x_full[sx], (j / XS) & 1, ctl)) {
                         ok = false;
                         break;
                     }
                     fence_after();
                     const int kk_end = (2 * j + 1 < nk64) ? 8 : 4;   // a stage may end with one 64-column unit
                     const uint32_t xaddr = smem_u32(xbuf + (size_t)sx * x_stage_bytes);
+                    const uint32_t a_t0 = tmem_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)hh * 64u;
                     for (int kk = 0; kk < kk_end; ++kk) {
-                        const uint32_t a_t =
-                            tmem_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)hh * 64u + (uint32_t)kk * 8u;
                         const uint32_t baddr =
                             xaddr + (uint32_t)(kk >> 2) * (uint32_t)mt * 128u + (uint32_t)(kk & 3) * 32u;
-                        mma_f16_tmem_a(tmem_base + acc_col, a_t, sw128_desc(baddr), idesc, acc_flag);
+                        mma_f16_tmem_a_warp(acc_tm, a_t0 + (uint32_t)kk * 8u, sw128_desc(baddr), idesc, acc_flag);
                         acc_flag = 1;
                     }
-                    mma_commit(&x_empty[sx]);
+                    mma_commit_warp(&x_empty[sx]);
                 }
                 if (!ok) break;
-                mma_commit(&a_empty[sa]);
+                mma_commit_warp(&a_empty[sa]);
             }
-            mma_commit(acc_full);   // completes when every MMA above has finished
+            mma_commit_warp(acc_full);   // completes when every MMA of every issuer has finished
             // no MMA may still run when tensor memory is freed
-            mbar_wait_drain(acc_full, 0, p.spin_limit, p.status);
+            if (lane == 0) mbar_wait_drain(acc_full, 0, p.spin_limit, p.status);
+            __syncwarp();
         }
-    } else if (warp == 3) {
-        // idle (keeps the role warps a multiple of 4)
     } else {
         // ---------------- dequantize, then epilogue ----------------
         const int dw = warp - kDequantWarp0;        // 0..7
@@ -608,11 +631,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t mrows = min((int64_t)mt, p.M - m0);
             const bool split = p.plan.slots() > 1;
             float* pslot = p.partials + (int64_t)piece * p.M * p.N;
+            const int nacc = nst < NI ? nst : NI;   // accumulators that received MMAs
             for (int c = 8 * half; c < mt; c += 16) {
                 uint32_t v[8];
                 __syncwarp();
                 tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)c, v);
                 tmem_ld_wait();
+                if (nacc > 1) {   // issuer 1's partial sum, added after issuer 0's
+                    uint32_t v1[8];
+                    tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)(mt + c), v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -719,7 +750,9 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     // kernel also takes all 512 tensor-memory columns. The shared-memory
     // request is kept above half of the SM's capacity.
     const int xs = mt > 128 ? 2 : (mt > 64 ? 4 : kMaxXStages);
-    int as = (kTmemCols - mt) / 128;
+    // two issuers (two accumulators) while they leave room for two A stages
+    const int ni = (tc::kMaxIssuers * mt + 2 * 128 <= kTmemCols) ? tc::kMaxIssuers : 1;
+    int as = (kTmemCols - ni * mt) / 128;
     as = as > kMaxAStages ? kMaxAStages : as;
     const size_t kBars = 512;
     const size_t x_bytes = (size_t)xs * mt * tc::kXBK * 2;
@@ -748,6 +781,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.x_stages = xs;
     p.w_stages = ws;
     p.a_stages = as;
+    p.n_issuers = ni;
     p.status = L.status;
     p.spin_limit = L.spin_limit;
 
