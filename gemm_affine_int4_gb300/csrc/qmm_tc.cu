@@ -22,16 +22,23 @@
 //               warp runs the issue loop (warp-uniform control flow) and
 //               elect.sync picks the lane that issues: a converged warp issues
 //               MMAs about twice as fast as one divergent lane. With two
-//               issuers, issuer j takes the stages i = j (mod 2) into its own
-//               accumulator, and the epilogue adds the two in a fixed order.
-//   warps 4-11  dequantize: thread t of warp quadrant q owns weight row
-//               32q + t and half of the stage's 128 K columns; it decodes the
-//               codes, computes w_hat = fma(q, s, b) in bf16x2/f16x2 (one
+//               issuers, issuer h takes the K half h (one activation stage) of
+//               every weight stage into its own accumulator, so a stage's MMAs
+//               run on both at once; the epilogue adds the two accumulators in
+//               a fixed order.
+//   warps 4-19  dequantize: thread t of a warp in lane quadrant q owns weight
+//               row 32q + t and one 64-column quarter of the stage; it decodes
+//               the codes, computes w_hat = fma(q, s, b) in bf16x2/f16x2 (one
 //               rounding of the exact value) and stores the row slice straight
-//               into tensor memory with tcgen05.st (the A ring, kAStages), so
-//               the weights never pass through shared memory a second time.
+//               into tensor memory with tcgen05.st (the A ring), so the
+//               weights never pass through shared memory a second time.
 //               After the K loop the same warps read the accumulator
 //               (tcgen05.ld) and write fp32 partials or the rounded output.
+// Scales and biases of a stage arrive by TMA with its packed weights (same
+// barrier) when the row length K / group_size is a multiple of 8; otherwise
+// the dequantize warps read them from global memory. Keeping global loads out
+// of the dequantize warps matters: every mbarrier arrive (a release) waits
+// for all of the thread's outstanding loads.
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // GAI4_ERR_TIMEOUT in the device status word, lets the other roles drain, frees
 // its tensor memory and returns.
@@ -39,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -111,7 +119,10 @@ bool uniform_plan(int64_t N, int64_t K, int gs, int S, SplitPlan* out) {
 SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
     SplitPlan p;
     p.tiles = (int)((N + 127) / 128);
-    p.unit = gs > 64 ? gs : 64;
+    // 256-column cuts when K allows: every stage of the tensor-core kernel then
+    // starts on a 256-column boundary, so a stage's groups lie in one aligned
+    // 8-group box of scales / biases
+    p.unit = (K % 256 == 0 && gs <= 256) ? 256 : (gs > 64 ? gs : 64);
     p.s_base = 1;
     p.n_extra = 0;
     const int cap = std::min(max_pieces(K, p.unit), std::max(1, max_slots));
@@ -154,13 +165,14 @@ constexpr int kBK = 256;         // K columns per weight / A stage
 constexpr int kXBK = 128;        // K columns per activation stage (two 64-column swizzle atoms)
 constexpr int kMaxWStages = 8;   // packed-weight ring (runtime depth <= this)
 constexpr int kMaxAStages = 3;   // tensor-memory A ring (128 columns each; runtime depth <= this)
-constexpr int kMaxXStages = 6;   // activation ring (runtime depth <= this)
+constexpr int kMaxXStages = 8;   // activation ring (runtime depth <= this)
 constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
 constexpr int kTmemCols = 512;   // one CTA per SM owns all of tensor memory
 constexpr int kMaxIssuers = 2;   // MMA issuer warps (2 and 3), one accumulator each
-constexpr int kDequantWarps = 8;    // 2 per tensor-memory lane quadrant, 128 columns each
+constexpr int kDequantWarps = 16;   // 4 per tensor-memory lane quadrant, 64 columns each
 constexpr int kDequantWarp0 = 4;
 constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
+constexpr uint32_t kSbBox = 8 * kTileN * 2;    // one TMA box of scales or biases: 8 groups x 128 rows, u16
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -352,6 +364,7 @@ struct Params {
     int w_stages;
     int a_stages;
     int n_issuers;        // MMA issuer warps = accumulators (1 or 2)
+    int sb_boxes;         // 8-group boxes per stage and tensor reserved in shared memory (1 or 2)
     int* status;
     long long spin_limit;
 };
@@ -395,9 +408,19 @@ __device__ __forceinline__ void dequant_word4(uint32_t w, uint32_t s2, uint32_t 
     o[3] = __byte_perm(r[2], r[3], 0x7632);   // (w6, w7)
 }
 
-template <bool BF>
+// stage i's groups [g_first, g_last] lie in one or two 8-group TMA boxes
+// starting at group x0 (a multiple of 8: 16-byte aligned box origin)
+__device__ __forceinline__ void stage_groups(int64_t kst, int ncols, int lg, int& x0, int& nbox) {
+    const int g_first = (int)(kst >> lg);
+    const int g_last = (int)((kst + ncols - 1) >> lg);
+    x0 = g_first & ~7;
+    nbox = (g_last - x0) / 8 + 1;
+}
+
+template <bool BF, bool SBT>
 __global__ void __launch_bounds__(kThreads, 1)
     qmm_tc4_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap bmap,
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (128-byte swizzle atoms)
@@ -409,7 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t w_stage_bytes = kTileN * kBK / 2;           // 4-bit codes, 128-byte rows
     uint8_t* xbuf = smem;
     uint8_t* wbuf = xbuf + (size_t)XS * x_stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + (size_t)WS * w_stage_bytes);
+    const uint32_t sb_stage_bytes = 2u * kSbBox * (uint32_t)p.sb_boxes;
+    uint8_t* sbbuf = wbuf + (size_t)WS * w_stage_bytes;       // SBT: per W stage, scales then biases
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sbbuf + (SBT ? (size_t)WS * sb_stage_bytes : 0));
     uint64_t* w_full = bars;
     uint64_t* w_empty = w_full + kMaxWStages;
     uint64_t* x_full = w_empty + kMaxWStages;
@@ -441,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < AS; ++i) {
             mbar_init(&a_full[i], kDequantWarps);
-            mbar_init(&a_empty[i], 1);
+            mbar_init(&a_empty[i], p.n_issuers);   // one commit per issuer
         }
         mbar_init(acc_full, p.n_issuers);         // one commit per issuer
         *abort_flag = 0;
@@ -470,10 +495,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < nst; ++i) {
                 const int s = i % WS;
                 if (!mbar_wait(&w_empty[s], ((i / WS) & 1) ^ 1, ctl)) break;
-                mbar_arrive_expect_tx(&w_full[s], w_stage_bytes);
+                const int64_t kst = k_begin + (int64_t)kBK * i;
+                int x0 = 0, nbox = 0;
+                if constexpr (SBT) stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
+                mbar_arrive_expect_tx(&w_full[s], w_stage_bytes + 2u * kSbBox * (uint32_t)nbox);
                 // x coordinate in 32-bit words: (k_begin + 256 i) * 4 / 32
-                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)((k_begin + kBK * i) / 8),
-                            (int)n0);
+                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst / 8), (int)n0);
+                if constexpr (SBT) {
+                    uint8_t* sb = sbbuf + (size_t)s * sb_stage_bytes;
+                    for (int bx = 0; bx < nbox; ++bx) {
+                        tma_load_2d(sb + bx * kSbBox, &smap, &w_full[s], x0 + 8 * bx, (int)n0);
+                        tma_load_2d(sb + (uint32_t)p.sb_boxes * kSbBox + bx * kSbBox, &bmap, &w_full[s], x0 + 8 * bx,
+                                    (int)n0);
+                    }
+                }
                 ++issued;
             }
             // drain: every issued copy has landed before the CTA may exit
@@ -504,15 +539,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = make_idesc(BF ? 1 : 0, mt);
             const uint32_t acc_tm = tmem_base + acc_col + (uint32_t)(jw * mt);
             uint32_t acc_flag = 0;
-            for (int i = jw; i < nst; i += NI) {
-                const int sa = i % AS;
-                if (!warp_wait(&a_full[sa], (i / AS) & 1, ctl)) break;
+            const int hh0 = NI == 2 ? jw : 0, hh1 = NI == 2 ? jw + 1 : 2;
+            int sa = 0, pa = 0;
+            const int xstep = hh1 - hh0 == 1 ? 2 : 1;   // activation stages between this issuer's consecutive ones
+            int sx = hh0, px = 0;                       // slot / parity of this issuer's next activation stage
+            for (int i = 0; i < nst; ++i) {
+                if (!warp_wait(&a_full[sa], (uint32_t)pa, ctl)) break;
                 bool ok = true;
-                for (int hh = 0; hh < 2; ++hh) {        // the two activation stages of this A stage
+                for (int hh = hh0; hh < hh1; ++hh) {    // this issuer's activation stage(s) of this A stage
                     const int j = 2 * i + hh;
                     if (j >= nxs) break;
-                    const int sx = j % XS;
-                    if (!warp_wait(&x_full[sx], (j / XS) & 1, ctl)) {
+                    if (!warp_wait(&x_full[sx], (uint32_t)px, ctl)) {
                         ok = false;
                         break;
                     }
@@ -527,9 +564,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc_flag = 1;
                     }
                     mma_commit_warp(&x_empty[sx]);
+                    sx += xstep;
+                    if (sx >= XS) {
+                        sx -= XS;
+                        px ^= 1;
+                    }
                 }
                 if (!ok) break;
                 mma_commit_warp(&a_empty[sa]);
+                if (++sa == AS) {
+                    sa = 0;
+                    pa ^= 1;
+                }
             }
             mma_commit_warp(acc_full);   // completes when every MMA of every issuer has finished
             // no MMA may still run when tensor memory is freed
@@ -538,101 +584,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- dequantize, then epilogue ----------------
-        const int dw = warp - kDequantWarp0;        // 0..7
+        const int dw = warp - kDequantWarp0;        // 0..15
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
-        const int half = dw >> 2;                   // which 128 of the stage's 256 columns
+        const int part = dw >> 2;                   // which 64 of the stage's 256 columns
         const int r = quad * 32 + lane;             // weight row within the tile
         const int64_t row = n0 + r;
         const bool row_ok = row < p.N;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const uint16_t* srow = p.scales + row * p.groups;
-        const uint16_t* brow = p.biases + row * p.groups;
+        const uint16_t* srow = p.scales + (row_ok ? row : 0) * p.groups;
+        const uint16_t* brow = p.biases + (row_ok ? row : 0) * p.groups;
         const uint8_t* wrow = wbuf + (size_t)r * 128;
+        const int lg = p.gs_log2;
 
-        // scale / bias of the four 32-column quarters of this thread's 128
-        // columns (a quarter lies in one group), loaded two stages before use
-        auto load_sb = [&](int i, uint32_t (&sv)[4], uint32_t (&bv)[4]) {
+        // scale / bias of the two 32-column halves of this thread's 64 columns
+        // (a half lies in one group), read from global memory two stages
+        // ahead when they do not come by TMA
+        auto load_sb = [&](int i, uint32_t (&sv)[2], uint32_t (&bv)[2]) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                sv[q] = 0u;
-                bv[q] = 0u;
-                const int unit = 4 * i + 2 * half + (q >> 1);   // 64-column unit of this quarter
-                if (i < nst && unit < nk64 && row_ok) {
-                    const int64_t g = (k_begin + (int64_t)kBK * i + 128 * half + 32 * q) >> p.gs_log2;
-                    sv[q] = __ldg(srow + g);
-                    bv[q] = __ldg(brow + g);
+            for (int h = 0; h < 2; ++h) {
+                sv[h] = 0u;
+                bv[h] = 0u;
+                if (i < nst && 4 * i + part < nk64 && row_ok) {
+                    const int64_t g = (k_begin + (int64_t)kBK * i + 64 * part + 32 * h) >> lg;
+                    sv[h] = __ldg(srow + g);
+                    bv[h] = __ldg(brow + g);
                 }
             }
         };
-        uint32_t s0[4], b0[4], s1[4], b1[4];
-        load_sb(0, s0, b0);
-        load_sb(1, s1, b1);
+        uint32_t s0[2] = {0u, 0u}, b0[2] = {0u, 0u}, s1[2] = {0u, 0u}, b1[2] = {0u, 0u};
+        if constexpr (!SBT) {
+            load_sb(0, s0, b0);
+            load_sb(1, s1, b1);
+        }
 
+        int sw = 0, pw = 0, sa = 0, pa = 0;   // ring slots and phase parities of stage i
         for (int i = 0; i < nst; ++i) {
-            const int sw = i % WS, sa = i % AS;
-            uint32_t sc[4], bc[4];
+            const bool active = 4 * i + part < nk64;   // the last stage may hold fewer 64-column units
+            uint32_t sc[2], bc[2];
+            if constexpr (!SBT) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                sc[q] = s0[q];
-                bc[q] = b0[q];
-                s0[q] = s1[q];
-                b0[q] = b1[q];
+                for (int h = 0; h < 2; ++h) {
+                    sc[h] = s0[h];
+                    bc[h] = b0[h];
+                    s0[h] = s1[h];
+                    b0[h] = b1[h];
+                }
+                load_sb(i + 2, s1, b1);
             }
-            load_sb(i + 2, s1, b1);
-            if (!warp_wait(&w_full[sw], (i / WS) & 1, ctl)) break;
-            // this thread's 64 bytes (128 codes) of the row: 128-byte rows,
+            if (!warp_wait(&w_full[sw], (uint32_t)pw, ctl)) break;
+            // this thread's 32 bytes (64 codes) of the row: 128-byte rows,
             // 128-byte TMA swizzle (16-byte chunk c of row r at chunk c ^ (r & 7))
-            uint4 v[4];
             const uint8_t* rowp = wrow + (size_t)sw * w_stage_bytes;
+            const uint4 va = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * part) ^ (r & 7)));
+            const uint4 vb = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * part + 1) ^ (r & 7)));
+            if constexpr (SBT) {
+                const int64_t kst = k_begin + (int64_t)kBK * i;
+                int x0, nbox;
+                stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), lg, x0, nbox);
+                const uint8_t* sb = sbbuf + (size_t)sw * sb_stage_bytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                v[c] = *reinterpret_cast<const uint4*>(rowp + 16 * ((4 * half + c) ^ (r & 7)));
+                for (int h = 0; h < 2; ++h) {
+                    // group of this half, relative to the box origin: box (idx >> 3), column (idx & 7)
+                    const int idx = active ? (int)((kst + 64 * part + 32 * h) >> lg) - x0 : 0;
+                    const uint32_t off = (uint32_t)(idx >> 3) * kSbBox + (uint32_t)r * 16u + 2u * (uint32_t)(idx & 7);
+                    sc[h] = *reinterpret_cast<const uint16_t*>(sb + off);
+                    bc[h] = *reinterpret_cast<const uint16_t*>(sb + (uint32_t)p.sb_boxes * kSbBox + off);
+                }
+            }
             // the stage is refilled by TMA (async proxy): order these generic
             // reads before that write, then release the stage
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[sw]);
 
-            if (!warp_wait(&a_empty[sa], ((i / AS) & 1) ^ 1, ctl)) break;
+            if (!warp_wait(&a_empty[sa], (uint32_t)(pa ^ 1), ctl)) break;
             fence_after();
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {    // two 64-column units -> 32 TMEM columns each
-                const int unit = 4 * i + 2 * half + sub;
-                if (unit < nk64) {
-                    uint32_t o[32];
-                    const uint32_t s2a = sc[2 * sub] | (sc[2 * sub] << 16), b2a = bc[2 * sub] | (bc[2 * sub] << 16);
-                    const uint32_t s2b = sc[2 * sub + 1] | (sc[2 * sub + 1] << 16);
-                    const uint32_t b2b = bc[2 * sub + 1] | (bc[2 * sub + 1] << 16);
-                    const uint4 va = v[2 * sub], vb = v[2 * sub + 1];
-                    dequant_word4<BF>(va.x, s2a, b2a, &o[0]);
-                    dequant_word4<BF>(va.y, s2a, b2a, &o[4]);
-                    dequant_word4<BF>(va.z, s2a, b2a, &o[8]);
-                    dequant_word4<BF>(va.w, s2a, b2a, &o[12]);
-                    dequant_word4<BF>(vb.x, s2b, b2b, &o[16]);
-                    dequant_word4<BF>(vb.y, s2b, b2b, &o[20]);
-                    dequant_word4<BF>(vb.z, s2b, b2b, &o[24]);
-                    dequant_word4<BF>(vb.w, s2b, b2b, &o[28]);
-                    tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)half * 64u +
-                                  (uint32_t)sub * 32u,
-                              o);
-                }
+            if (active) {
+                uint32_t o[32];
+                const uint32_t s2a = sc[0] | (sc[0] << 16), b2a = bc[0] | (bc[0] << 16);
+                const uint32_t s2b = sc[1] | (sc[1] << 16), b2b = bc[1] | (bc[1] << 16);
+                dequant_word4<BF>(va.x, s2a, b2a, &o[0]);
+                dequant_word4<BF>(va.y, s2a, b2a, &o[4]);
+                dequant_word4<BF>(va.z, s2a, b2a, &o[8]);
+                dequant_word4<BF>(va.w, s2a, b2a, &o[12]);
+                dequant_word4<BF>(vb.x, s2b, b2b, &o[16]);
+                dequant_word4<BF>(vb.y, s2b, b2b, &o[20]);
+                dequant_word4<BF>(vb.z, s2b, b2b, &o[24]);
+                dequant_word4<BF>(vb.w, s2b, b2b, &o[28]);
+                tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)part * 32u, o);
             }
             tmem_st_wait();
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[sa]);
+            if (++sw == WS) {
+                sw = 0;
+                pw ^= 1;
+            }
+            if (++sa == AS) {
+                sa = 0;
+                pa ^= 1;
+            }
         }
 
-        // epilogue: accumulator rows -> fp32 partials or T output; the 2 warps
-        // of a quadrant take 8-column chunks alternately
+        // epilogue: accumulator rows -> fp32 partials or T output; the 4 warps
+        // of a quadrant take 8-column chunks in turn
         const bool ok = warp_wait(acc_full, 0, ctl);
         fence_after();
         if (ok) {
             const int64_t mrows = min((int64_t)mt, p.M - m0);
             const bool split = p.plan.slots() > 1;
             float* pslot = p.partials + (int64_t)piece * p.M * p.N;
-            const int nacc = nst < NI ? nst : NI;   // accumulators that received MMAs
-            for (int c = 8 * half; c < mt; c += 16) {
+            const int nacc = nxs < NI ? nxs : NI;   // accumulators that received MMAs
+            for (int c = 8 * part; c < mt; c += 32) {
                 uint32_t v[8];
                 __syncwarp();
                 tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)c, v);
@@ -721,7 +785,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     const int mt = (int)((mrows + 15) / 16 * 16);
 
     // packed weights: u32 [N, K/8], box {32 words = 256 columns, 128 rows}, 128-byte swizzle
-    CUtensorMap wmap, xmap;
+    CUtensorMap wmap, xmap, smap, bmap;
     {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
@@ -744,21 +808,57 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
             return cudaErrorInvalidValue;
     }
 
+    // scales / biases: 16-bit [N, K / group_size], box {8 groups, 128 rows}
+    // (16-byte rows, no swizzle); the row stride must be a multiple of 16 bytes
+    const int64_t groups = K / L.group_size;
+    const bool sbt = groups % 8 == 0;
+    memset(&smap, 0, sizeof(smap));
+    memset(&bmap, 0, sizeof(bmap));
+    if (sbt) {
+        cuuint64_t dims[2] = {(cuuint64_t)groups, (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(groups * 2)};
+        cuuint32_t box[2] = {8, 128};
+        cuuint32_t es[2] = {1, 1};
+        CUtensorMap* maps[2] = {&smap, &bmap};
+        const void* srcs[2] = {L.scales, L.biases};
+        for (int t = 0; t < 2; ++t)
+            if (enc(maps[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(srcs[t]), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+    }
+
     // Ring depths. One CTA per SM: a second co-resident CTA of this kernel
     // could run warps whose tensor-memory lane quadrant differs from
     // (warp index % 4), which the dequantize and epilogue roles rely on; the
     // kernel also takes all 512 tensor-memory columns. The shared-memory
     // request is kept above half of the SM's capacity.
-    const int xs = mt > 128 ? 2 : (mt > 64 ? 4 : kMaxXStages);
     // two issuers (two accumulators) while they leave room for two A stages
     const int ni = (tc::kMaxIssuers * mt + 2 * 128 <= kTmemCols) ? tc::kMaxIssuers : 1;
     int as = (kTmemCols - ni * mt) / 128;
     as = as > kMaxAStages ? kMaxAStages : as;
+    // one box of scales / biases per stage suffices when every piece starts on
+    // a 256-column boundary (then so does every stage)
+    int sb_boxes = 0;
+    if (sbt) {
+        bool aligned = true;
+        const int64_t KU = K / L.plan.unit;
+        for (int st = L.plan.s_base; st <= L.plan.s_base + (L.plan.n_extra > 0 ? 1 : 0); ++st)
+            for (int j = 0; j < st; ++j)
+                if (((j * KU / st) * L.plan.unit) % 256 != 0) aligned = false;
+        sb_boxes = aligned ? 1 : 2;
+    }
+    // Activation ring as deep as possible (up to 8) while it leaves four
+    // weight stages: activation tiles are re-read by every CTA from L2 and
+    // their latency needs the lookahead.
     const size_t kBars = 512;
-    const size_t x_bytes = (size_t)xs * mt * tc::kXBK * 2;
-    const size_t w_stage = (size_t)kTileN * kBK / 2;
-    const size_t budget = 210 * 1024;
-    int ws = (int)((budget - 1024 - kBars - x_bytes) / w_stage);
+    const size_t x_stage = (size_t)mt * tc::kXBK * 2;
+    const size_t w_stage = (size_t)kTileN * kBK / 2 + 2u * tc::kSbBox * (size_t)sb_boxes;
+    const size_t budget = 224 * 1024 - 1024 - kBars;
+    int xs = (int)((budget - 4 * w_stage) / x_stage);
+    xs = xs < 2 ? 2 : (xs > kMaxXStages ? kMaxXStages : xs);
+    const size_t x_bytes = (size_t)xs * x_stage;
+    int ws = (int)((budget - x_bytes) / w_stage);
     ws = ws < 3 ? 3 : (ws > kMaxWStages ? kMaxWStages : ws);
     size_t smem = 1024 + x_bytes + (size_t)ws * w_stage + kBars;
     if (smem < 120 * 1024) smem = 120 * 1024;
@@ -782,21 +882,23 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.w_stages = ws;
     p.a_stages = as;
     p.n_issuers = ni;
+    p.sb_boxes = sb_boxes > 0 ? sb_boxes : 1;
     p.status = L.status;
     p.spin_limit = L.spin_limit;
 
-    auto kern = L.is_bf16 ? tc::qmm_tc4_kernel<true> : tc::qmm_tc4_kernel<false>;
-    static unsigned long long configured[2] = {0ull, 0ull};
+    auto kern = L.is_bf16 ? (sbt ? tc::qmm_tc4_kernel<true, true> : tc::qmm_tc4_kernel<true, false>)
+                          : (sbt ? tc::qmm_tc4_kernel<false, true> : tc::qmm_tc4_kernel<false, false>);
+    static unsigned long long configured[4] = {0ull, 0ull, 0ull, 0ull};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int which = L.is_bf16 ? 1 : 0;
+    const int which = (L.is_bf16 ? 1 : 0) + (sbt ? 2 : 0);
     if (dev >= 64 || !(configured[which] & (1ull << dev))) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[which] |= 1ull << dev;
     }
     dim3 grid((unsigned)L.plan.pieces(), 1u, (unsigned)mchunks);
-    kern<<<grid, kThreads, smem, stream>>>(wmap, xmap, p);
+    kern<<<grid, kThreads, smem, stream>>>(wmap, xmap, smap, bmap, p);
     return cudaGetLastError();
 }
 
