@@ -93,7 +93,7 @@ static cudaError_t launch_affine(const AffineGemvLaunch& L, int dtype, cudaStrea
 // ---------------------------------------------------------------------------
 // qmm_t planning: path (CUDA-core / tensor core) and K split
 // ---------------------------------------------------------------------------
-static const int64_t kTcMinM = 9;   // tensor-core path from this many x rows up (bf16/f16)
+static const int64_t kTcMinM = 3;   // tensor-core path from this many x rows up (bf16/f16; measured crossover)
 
 static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, int dtype, int split_k,
                             size_t ws_bytes, bool unlimited_ws, int* path, SplitPlan* plan) {

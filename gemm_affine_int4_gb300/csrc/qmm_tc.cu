@@ -71,20 +71,61 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ P, typename T::st
     out[i] = T::from_f32(acc);
 }
 
+// 8 consecutive outputs of one row per thread (N % 8 == 0, 16-byte aligned
+// partials and output): two 16-byte loads per partial slot, one store
+template <typename T>
+__global__ void splitk_reduce8_kernel(const float* __restrict__ P, typename T::storage* __restrict__ out, int64_t M,
+                                      int64_t N, SplitPlan plan) {
+    const int64_t MN = M * N;
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // chunk of 8 outputs
+    if (c >= MN / 8) return;
+    const int64_t i = c * 8;
+    const int64_t n = i % N;
+    const int tile = (int)(n / 128);   // 8 | 128: the chunk lies in one tile
+    const int s_t = plan.s_base + (tile < plan.n_extra ? 1 : 0);
+    float4 a = __ldcs(reinterpret_cast<const float4*>(P + i));
+    float4 b = __ldcs(reinterpret_cast<const float4*>(P + i + 4));
+    for (int s = 1; s < s_t; ++s) {
+        const float4 u = __ldcs(reinterpret_cast<const float4*>(P + (int64_t)s * MN + i));
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(P + (int64_t)s * MN + i + 4));
+        a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+        b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+    }
+    if constexpr (sizeof(typename T::storage) == 4) {
+        reinterpret_cast<float4*>(out + i)[0] = a;
+        reinterpret_cast<float4*>(out + i)[1] = b;
+    } else {
+        uint4 o;
+        o.x = (uint32_t)T::from_f32(a.x) | ((uint32_t)T::from_f32(a.y) << 16);
+        o.y = (uint32_t)T::from_f32(a.z) | ((uint32_t)T::from_f32(a.w) << 16);
+        o.z = (uint32_t)T::from_f32(b.x) | ((uint32_t)T::from_f32(b.y) << 16);
+        o.w = (uint32_t)T::from_f32(b.z) | ((uint32_t)T::from_f32(b.w) << 16);
+        *reinterpret_cast<uint4*>(out + i) = o;
+    }
+}
+
+template <typename T>
+static void reduce_launch(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
+                          cudaStream_t s) {
+    auto* o = static_cast<typename T::storage*>(out);
+    const int64_t MN = M * N;
+    const bool vec = N % 8 == 0 && (reinterpret_cast<uintptr_t>(partials) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    if (vec) {
+        const unsigned blocks = (unsigned)((MN / 8 + 255) / 256);
+        splitk_reduce8_kernel<T><<<blocks, 256, 0, s>>>(partials, o, M, N, plan);
+    } else {
+        const unsigned blocks = (unsigned)((MN + 255) / 256);
+        splitk_reduce_kernel<T><<<blocks, 256, 0, s>>>(partials, o, M, N, plan);
+    }
+}
+
 cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
                                  int dtype, cudaStream_t s) {
-    const int64_t MN = M * N;
-    const unsigned blocks = (unsigned)((MN + 255) / 256);
     switch (dtype) {
-    case GAI4_F16:
-        splitk_reduce_kernel<F16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), M, N, plan);
-        break;
-    case GAI4_F32:
-        splitk_reduce_kernel<F32><<<blocks, 256, 0, s>>>(partials, static_cast<float*>(out), M, N, plan);
-        break;
-    default:
-        splitk_reduce_kernel<BF16><<<blocks, 256, 0, s>>>(partials, static_cast<uint16_t*>(out), M, N, plan);
-        break;
+    case GAI4_F16: reduce_launch<F16>(partials, out, M, N, plan, s); break;
+    case GAI4_F32: reduce_launch<F32>(partials, out, M, N, plan, s); break;
+    default: reduce_launch<BF16>(partials, out, M, N, plan, s); break;
     }
     return cudaGetLastError();
 }
