@@ -90,6 +90,18 @@ static cudaError_t launch_affine(const AffineGemvLaunch& L, int dtype, cudaStrea
     }
 }
 
+// M = 1: the prefetching 4-bit kernel where it applies, else the general one
+static cudaError_t run_qmv(const uint32_t* w, const void* sc, const void* bi, const void* x, void* out, int dtype,
+                           int bits, int gs, int64_t N, int64_t K, cudaStream_t s) {
+    if (qmv4_supported(sc, bi, dtype, bits, gs, N, K)) {
+        int* st = status_ptr();
+        if (!st) return cudaErrorMemoryAllocation;
+        return launch_qmv4(w, sc, bi, x, out, dtype, gs, N, K, st, 2000000000LL, s);
+    }
+    const AffineGemvLaunch L = plan_affine(w, sc, bi, x, out, bits, gs, 1, N, K);
+    return launch_affine(L, dtype, s);
+}
+
 // ---------------------------------------------------------------------------
 // qmm_t planning: path (CUDA-core / tensor core) and K split
 // ---------------------------------------------------------------------------
@@ -174,8 +186,7 @@ gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* b
     if (st != GAI4_OK) return st;
     if (!w_packed || !scales || !biases || !x || !out) return GAI4_ERR_INVALID_ARG;
     if (!aligned16(w_packed) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
-    const AffineGemvLaunch L = plan_affine(w_packed, scales, biases, x, out, bits, group_size, 1, N, K);
-    return from_cuda(launch_affine(L, dtype, (cudaStream_t)stream));
+    return from_cuda(run_qmv(w_packed, scales, biases, x, out, dtype, bits, group_size, N, K, (cudaStream_t)stream));
 }
 
 size_t gai4_qmm_t_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits, int group_size, gai4_dtype dtype,
@@ -213,6 +224,7 @@ gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void*
     }
     cudaStream_t s = (cudaStream_t)stream;
     if (path == 0) {
+        if (M == 1) return from_cuda(run_qmv(w_packed, scales, biases, x, out, dtype, bits, group_size, N, K, s));
         const AffineGemvLaunch L = plan_affine(w_packed, scales, biases, x, out, bits, group_size, M, N, K);
         return from_cuda(launch_affine(L, dtype, s));
     }

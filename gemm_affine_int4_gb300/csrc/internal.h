@@ -26,6 +26,12 @@ cudaError_t launch_affine_gemv_bf16(const AffineGemvLaunch& L, cudaStream_t s);
 cudaError_t launch_affine_gemv_f16(const AffineGemvLaunch& L, cudaStream_t s);
 cudaError_t launch_affine_gemv_f32(const AffineGemvLaunch& L, cudaStream_t s);
 
+// CUDA-core qmv for 4-bit codes with per-lane asynchronous prefetch (qmv4.cu)
+int qmv4_supported(const void* scales, const void* biases, int dtype, int bits, int gs, int64_t N, int64_t K);
+cudaError_t launch_qmv4(const uint32_t* w, const void* scales, const void* biases, const void* x, void* out,
+                        int dtype, int gs, int64_t N, int64_t K, int* status, long long spin_limit,
+                        cudaStream_t s);
+
 // K-split plan of the tensor-core qmm_t. The N axis is cut into 128-row
 // tiles; tile t is cut along K into s_t pieces (s_t = s_base + 1 for the first
 // n_extra tiles, s_base for the rest), piece j of s_t covering K columns

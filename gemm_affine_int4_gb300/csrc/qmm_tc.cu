@@ -50,6 +50,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace gai4 {
 
@@ -201,6 +202,8 @@ SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
 // ---------------------------------------------------------------------------
 namespace tc {
 
+using namespace pipe;
+
 constexpr int kTileN = 128;      // weight rows per CTA (MMA M)
 constexpr int kBK = 256;         // K columns per weight / A stage
 constexpr int kXBK = 128;        // K columns per activation stage (two 64-column swizzle atoms)
@@ -214,83 +217,6 @@ constexpr int kDequantWarps = 16;   // 4 per tensor-memory lane quadrant, 64 col
 constexpr int kDequantWarp0 = 4;
 constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
 constexpr uint32_t kSbBox = 8 * kTileN * 2;    // one TMA box of scales or biases: 8 groups x 128 rows, u16
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-struct Ctl {
-    int* status;            // device status word
-    long long limit;        // clock64 cycles a single wait may take
-    volatile int* abort_;   // shared flag: some role gave up
-};
-
-// bounded wait: false after `limit` cycles (or when another role gave up)
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*c.abort_) return false;
-        if (clock64() - t0 > c.limit) {
-            *c.abort_ = 1;
-            atomicExch(c.status, (int)GAI4_ERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-// bounded wait that ignores the abort flag: used to drain copies and MMAs that
-// were already issued, so that no asynchronous write lands after the CTA exits
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > limit) {
-            atomicExch(status, (int)GAI4_ERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-// warp-uniform wait: every lane observes the phase itself (each lane's own
-// acquire makes the asynchronously written data visible to it), then the warp
-// reconverges (the following tcgen05 .sync.aligned instructions need every
-// lane, converged) and agrees on the outcome
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
-    const bool ok = mbar_wait(bar, parity, c);
-    __syncwarp();
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -793,21 +719,6 @@ using tc::kMaxXStages;
 using tc::kThreads;
 using tc::kTileN;
 using tc::kTmemCols;
-
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
 
 int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int gs) {
     (void)M;

@@ -1,0 +1,507 @@
+// qmv4.cu -- CUDA-core qmv (M = 1) for 4-bit codes, group size 32/64/128,
+// bf16 / f16 / f32 activations, binary32 accumulation.
+//
+// out[n] = sum_g ( s[n,g] * sum_{k in g} q[n,k] x[k] + b[n,g] * sum_{k in g} x[k] )
+// (metaltile-std quantized.rs, mt_qmv: the bias-hoist split of the affine dot
+// product; coalesced 128-bit weight reads, x reused across rows, warp-shuffle
+// reduction.)
+//
+// GB300 design:
+//  * One CTA per SM, persistent over blocks of BR = (16 / S) * R rows: 16
+//    consumer warps and one producer warp. A consumer warp owns R rows of a
+//    block; S warps split the 1024-column iterations of a row group when rows
+//    alone would leave SMs idle. A lane owns 32 consecutive codes (16 bytes)
+//    of each of its rows per iteration.
+//  * The producer's elected thread streams each stage -- S iterations of the
+//    block's packed weights, scales and biases -- into a ring of shared-memory
+//    stages (full / empty mbarriers, zero fill past N). When K is a multiple
+//    of 1024 the tensors are viewed as [rows][iterations][columns] and one
+//    3-D TMA box per tensor brings a whole stage; otherwise one 2-D box per
+//    iteration (zero fill past K). Consumer lanes issue no copies and no
+//    global loads in the loop.
+//  * x is staged once per CTA in binary32, permuted so that a warp's 16-byte
+//    reads are contiguous, with per-chunk sums for the bias term.
+//  * A code becomes a number through the mantissa of 1.0f: one shift places
+//    two codes at mantissa bits 15..18 and 19..22, and one three-input logic
+//    op each (mask, then the exponent of 1.0f) gives the floats 1 + q/256 and
+//    1 + q/16 exactly. Per 32-bit word of 8 codes: 4 shifts, 8 logic ops and 8
+//    fmas, into an even-code and an odd-code accumulator that start at
+//    -sum x_even and -sum x_odd of the chunk, so that
+//    256 * acc_even + 16 * acc_odd is the chunk's sum q x.
+#include <algorithm>
+#include <initializer_list>
+
+#include "common.cuh"
+#include "internal.h"
+#include "pipeline.cuh"
+
+namespace gai4 {
+
+namespace {
+
+using namespace pipe;
+
+constexpr int kCWarps = 16;                        // consumer warps
+constexpr int kThreads = 32 * (kCWarps + 1);       // + one producer warp
+constexpr int kItCols = 1024;                      // columns of one warp iteration (32 lanes x 32 codes)
+constexpr int kMaxDepth = 8;
+constexpr uint32_t kOne = 0x3F800000u;             // 1.0f
+constexpr uint32_t kMaskLo = 0x00078000u;          // code at mantissa bits 15..18 -> 1 + q/256
+constexpr uint32_t kMaskHi = 0x00780000u;          // code at mantissa bits 19..22 -> 1 + q/16
+
+struct Qmv4Args {
+    const void* x;
+    void* out;
+    int64_t N, K;
+    int gs_log2;
+    int S;                  // warps splitting the iterations of one row group
+    int n_it;               // iterations per row: ceil(K / 1024)
+    int n_st;               // stages per block: ceil(n_it / S)
+    int depth;              // ring depth
+    int64_t n_blocks;       // row blocks
+    int sbg;                // groups per iteration: 1024 / group_size
+    uint32_t w_slice;       // bytes of one iteration's packed weights in a stage: BR * 512
+    uint32_t sb_slice;      // bytes of one iteration's scales (or biases), padded to 128
+    uint32_t stage_bytes;   // S * (w_slice + 2 * sb_slice)
+    int box3;               // 1: one 3-D box per tensor and stage, layout [row][iteration][...]
+    uint32_t w_rs, w_is;    // byte strides of a row and of an iteration in a stage's packed weights
+    uint32_t sb_rs, sb_is;  // element strides of a row and of an iteration in a stage's scales / biases
+    uint32_t mask_lo, mask_hi, one;   // operands of the three-input logic op, kept in registers
+    int flush;              // row blocks whose partial sums are held in shared memory between flushes
+    int* status;
+    long long spin_limit;
+};
+
+// (a & b) | c as one three-input logic instruction
+__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    qmv4_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+                const __grid_constant__ CUtensorMap bmap, const Qmv4Args a) {
+    using St = typename T::storage;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte aligned base (TMA destinations); pointer arithmetic on the
+    // shared array keeps the accesses below in the shared state space
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const int n_it = a.n_it, D = a.depth, S = a.S, n_st = a.n_st;
+    const int G = kCWarps / S, BR = G * R;
+    float4* xs = reinterpret_cast<float4*>(smem);                     // [n_it][8][32] permuted x
+    float4* cs = xs + (size_t)n_it * 256;                             // [n_it * 32] chunk constants
+    uint8_t* ring = reinterpret_cast<uint8_t*>(cs + (size_t)n_it * 32);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)D * a.stage_bytes);
+    uint64_t* empty = full + kMaxDepth;
+    float* pend = reinterpret_cast<float*>(empty + kMaxDepth);        // [flush][kCWarps * R] partial sums
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(pend + (size_t)a.flush * kCWarps * R);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t my_blocks =
+        a.n_blocks > (int64_t)blockIdx.x ? (a.n_blocks - 1 - (int64_t)blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < D; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCWarps);   // one arrive per consumer warp
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    Ctl ctl{a.status, a.spin_limit, abort_flag};
+
+    if (warp == kCWarps) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int slot = 0, ph = 0;
+            int64_t issued = 0;
+            for (int64_t b = 0; b < my_blocks; ++b) {
+                const int row0 = (int)(((int64_t)blockIdx.x + b * gridDim.x) * BR);
+                for (int j = 0; j < n_st; ++j) {
+                    if (!mbar_wait(&empty[slot], (uint32_t)(ph ^ 1), ctl)) goto drain;
+                    const int it0 = j * S;
+                    const int nsl = min(S, n_it - it0);   // iterations present in this stage
+                    // a 3-D box always lands whole (iterations past the row are zero-filled)
+                    const uint32_t n_its = a.box3 ? (uint32_t)S : (uint32_t)nsl;
+                    mbar_arrive_expect_tx(&full[slot],
+                                          n_its * (a.w_slice + 2u * (uint32_t)BR * (uint32_t)a.sbg *
+                                                                   (uint32_t)sizeof(St)));
+                    uint8_t* st = ring + (size_t)slot * a.stage_bytes;
+                    if (a.box3) {
+                        tma_load_3d(st, &wmap, &full[slot], 0, it0, row0);
+                        uint8_t* sbs = st + (size_t)S * a.w_slice;
+                        tma_load_3d(sbs, &smap, &full[slot], 0, it0, row0);
+                        tma_load_3d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], 0, it0, row0);
+                    } else for (int ss = 0; ss < nsl; ++ss) {
+                        const int it = it0 + ss;
+                        tma_load_2d(st + ss * a.w_slice, &wmap, &full[slot], it * (kItCols / 8), row0);
+                        uint8_t* sbs = st + (size_t)S * a.w_slice + (size_t)ss * a.sb_slice;
+                        tma_load_2d(sbs, &smap, &full[slot], it * a.sbg, row0);
+                        tma_load_2d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], it * a.sbg, row0);
+                    }
+                    ++issued;
+                    if (++slot == D) {
+                        slot = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+        drain:
+            // every issued copy has landed before the CTA may exit
+            for (int64_t q = (issued > D ? issued - D : 0); q < issued; ++q)
+                mbar_wait_drain(&full[q % D], (uint32_t)((q / D) & 1), a.spin_limit, a.status);
+        }
+        return;
+    }
+
+    // ---------------- consumers: stage x once ----------------
+    const St* xg = static_cast<const St*>(a.x);
+    const int64_t K = a.K;
+    for (int c = threadIdx.x; c < n_it * 32; c += kCWarps * 32) {
+        float v[32];
+        const int64_t k0 = (int64_t)c * 32;
+        if (k0 < K) {   // K is a multiple of 32: a chunk is all in or all out
+            if constexpr (T::kBytes == 4) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 f = *reinterpret_cast<const float4*>(xg + k0 + 4 * j);
+                    v[4 * j] = f.x;
+                    v[4 * j + 1] = f.y;
+                    v[4 * j + 2] = f.z;
+                    v[4 * j + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(xg + k0 + 8 * j);
+                    const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        v[8 * j + 2 * h] = T::to_f32((uint16_t)(uu[h] & 0xFFFFu));
+                        v[8 * j + 2 * h + 1] = T::to_f32((uint16_t)(uu[h] >> 16));
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        float xe = 0.f, xo = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            xe += v[2 * j];
+            xo += v[2 * j + 1];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            xs[((c >> 5) * 8 + j) * 32 + (c & 31)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        cs[c] = make_float4(-xe, -xo, xe + xo, 0.f);
+    }
+    consumer_bar();
+
+    // ---------------- consumers: main loop ----------------
+    const int g = warp / S, sl = warp % S;
+    const uint32_t mlo = a.mask_lo, mhi = a.mask_hi, one = a.one;
+    const int grp_off = (lane * 32) >> a.gs_log2;   // this lane's group within an iteration
+    St* out = static_cast<St*>(a.out);
+    int slot = 0, ph = 0;
+    for (int64_t b = 0; b < my_blocks; ++b) {
+        float part[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) part[r] = 0.f;
+        for (int j = 0; j < n_st; ++j) {
+            const int it = j * S + sl;
+            const bool ok = warp_wait(&full[slot], (uint32_t)ph, ctl);
+            if (ok && it < n_it) {
+                const uint8_t* st = ring + (size_t)slot * a.stage_bytes;
+                const uint8_t* wsl = st + (size_t)sl * a.w_is + (size_t)(g * R) * a.w_rs + lane * 16;
+                const St* ssl = reinterpret_cast<const St*>(st + (size_t)S * a.w_slice) + sl * a.sb_is +
+                                (g * R) * a.sb_rs + grp_off;
+                const St* bsl = ssl + (size_t)S * a.sb_slice / sizeof(St);
+                uint4 wv[R];
+                float sc[R], bc[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    wv[r] = *reinterpret_cast<const uint4*>(wsl + r * a.w_rs);
+                    sc[r] = T::to_f32(ssl[r * a.sb_rs]);
+                    bc[r] = T::to_f32(bsl[r * a.sb_rs]);
+                }
+                // the slot is refilled by TMA (async proxy): order these reads first, then release it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+
+                const float4 cst = cs[it * 32 + lane];
+                float ae[R], ao[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    ae[r] = cst.x;
+                    ao[r] = cst.y;
+                }
+#pragma unroll
+                for (int tw = 0; tw < 4; ++tw) {
+                    const float4 p0 = xs[(it * 8 + 2 * tw) * 32 + lane];
+                    const float4 p1 = xs[(it * 8 + 2 * tw + 1) * 32 + lane];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
+                        uint32_t u = w << 15;   // codes 0, 1
+                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p0.x, ae[r]);
+                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p0.y, ao[r]);
+                        u = w << 7;             // codes 2, 3
+                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p0.z, ae[r]);
+                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p0.w, ao[r]);
+                        u = w >> 1;             // codes 4, 5
+                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p1.x, ae[r]);
+                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p1.y, ao[r]);
+                        u = w >> 9;             // codes 6, 7
+                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p1.z, ae[r]);
+                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p1.w, ao[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float qx = fmaf(256.f, ae[r], 16.f * ao[r]);   // sum q x of the chunk
+                    part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.z, part[r]));
+                }
+            } else {
+                // nothing to read (an iteration past K, or a wait that gave up): release the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            if (++slot == D) {
+                slot = 0;
+                ph ^= 1;
+            }
+        }
+        // the warp's row sums, held until the next flush; a flush adds the S
+        // warps of each row group in a fixed order and writes the rows (no
+        // barrier or global store inside the stage loop: a store would make
+        // the next mbarrier arrive wait for it)
+        const int bl = (int)(b % a.flush);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float v = warp_sum(part[r]);
+            if (lane == 0) pend[(size_t)bl * (kCWarps * R) + warp * R + r] = v;
+        }
+        if (bl == a.flush - 1 || b == my_blocks - 1) {
+            consumer_bar();
+            const int64_t b0 = b - bl;
+            for (int t = threadIdx.x; t < (bl + 1) * BR; t += kCWarps * 32) {
+                const int bb = t / BR, rr = t - bb * BR;
+                const int gg = rr / R, r = rr - gg * R;
+                const float* pb = pend + (size_t)bb * (kCWarps * R);
+                float v = 0.f;
+                for (int ss = 0; ss < S; ++ss) v += pb[(gg * S + ss) * R + r];
+                const int64_t row = ((int64_t)blockIdx.x + (b0 + bb) * gridDim.x) * BR + rr;
+                if (row < a.N) out[row] = T::from_f32(v);
+            }
+            consumer_bar();
+        }
+    }
+}
+
+// (R, S): per stage a CTA spends about max(producer issue, one iteration of R
+// rows per warp) -- roughly max(800, 400 R) cycles -- so the busiest SM takes
+// ceil(blocks / SMs) * ceil(n_it / S) * max(2, R) units; ties go to more rows
+// per warp, then to fewer K splits
+struct Qmv4Plan {
+    int R, S, depth, flush;
+    int64_t n_blocks;
+    uint32_t w_slice, sb_slice, stage_bytes;
+    size_t smem;
+};
+
+bool plan_qmv4(int64_t N, int64_t K, int gs, int tbytes, Qmv4Plan* out) {
+    const int sms = num_sms();
+    const int n_it = (int)((K + kItCols - 1) / kItCols);
+    const int sbg = kItCols / gs;
+    const size_t fixed = (size_t)n_it * (256 + 32) * 16;   // x pieces + chunk constants
+    const size_t cap = 227 * 1024;
+    bool found = false;
+    int64_t best = 0;
+    for (int R : {4, 2, 1}) {
+        for (int S : {1, 2, 4, 8, 16}) {
+            const int BR = (kCWarps / S) * R;
+            const uint32_t w_slice = (uint32_t)BR * 512;
+            const uint32_t sb_slice = ((uint32_t)BR * sbg * tbytes + 127) / 128 * 128;
+            const uint32_t stage = (uint32_t)S * (w_slice + 2 * sb_slice);
+            const int64_t nb = (N + BR - 1) / BR;
+            const int64_t per_cta = (nb + sms - 1) / sms;
+            // pending partial sums: all of a CTA's blocks if they fit in 16 KB
+            const int64_t pend_row = (int64_t)kCWarps * R * 4;
+            const int flush = (int)std::max<int64_t>(1, std::min<int64_t>(per_cta, (16 * 1024) / pend_row));
+            const size_t tail = 2 * kMaxDepth * 8 + (size_t)flush * pend_row + 16 + 128;   // + alignment
+            if (fixed + tail + 2 * (size_t)stage > cap) continue;
+            const int depth = (int)std::min<size_t>(kMaxDepth, (cap - fixed - tail) / stage);
+            const int64_t cost = per_cta * ((n_it + S - 1) / S) * std::max(2, R);
+            if (!found || cost < best) {
+                found = true;
+                best = cost;
+                out->R = R;
+                out->S = S;
+                out->depth = depth;
+                out->flush = flush;
+                out->n_blocks = nb;
+                out->w_slice = w_slice;
+                out->sb_slice = sb_slice;
+                out->stage_bytes = stage;
+                out->smem = fixed + (size_t)depth * stage + tail;
+            }
+        }
+    }
+    return found;
+}
+
+template <typename T, int R>
+cudaError_t launch_t(const CUtensorMap& wm, const CUtensorMap& sm, const CUtensorMap& bm, const Qmv4Args& a,
+                     size_t smem, cudaStream_t s) {
+    static unsigned long long configured = 0ull;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(configured & (1ull << dev))) {
+        cudaError_t e =
+            cudaFuncSetAttribute(qmv4_kernel<T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured |= 1ull << dev;
+    }
+    const int64_t grid = std::min<int64_t>(a.n_blocks, num_sms());
+    qmv4_kernel<T, R><<<(unsigned)grid, kThreads, smem, s>>>(wm, sm, bm, a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_r(const CUtensorMap& wm, const CUtensorMap& sm, const CUtensorMap& bm, const Qmv4Args& a,
+                     int R, size_t smem, cudaStream_t s) {
+    switch (R) {
+    case 4: return launch_t<T, 4>(wm, sm, bm, a, smem, s);
+    case 2: return launch_t<T, 2>(wm, sm, bm, a, smem, s);
+    default: return launch_t<T, 1>(wm, sm, bm, a, smem, s);
+    }
+}
+
+}  // namespace
+
+int qmv4_supported(const void* scales, const void* biases, int dtype, int bits, int gs, int64_t N, int64_t K) {
+    if (bits != 4 || (gs != 32 && gs != 64 && gs != 128)) return 0;
+    if (K < kItCols) return 0;   // tensor extents at least one box wide
+    // TMA: 16-byte aligned bases and row strides (K / group_size scales per row)
+    if ((reinterpret_cast<uintptr_t>(scales) & 15) || (reinterpret_cast<uintptr_t>(biases) & 15)) return 0;
+    const int tbytes = dtype == GAI4_F32 ? 4 : 2;
+    if (((K / gs) * tbytes) % 16 != 0) return 0;
+    if (N > (int64_t)INT32_MAX || K / 8 > (int64_t)INT32_MAX) return 0;   // TMA coordinates are 32-bit
+    if (!encode_fn()) return 0;
+    Qmv4Plan p;
+    return plan_qmv4(N, K, gs, tbytes, &p) ? 1 : 0;
+}
+
+cudaError_t launch_qmv4(const uint32_t* w, const void* scales, const void* biases, const void* x, void* out,
+                        int dtype, int gs, int64_t N, int64_t K, int* status, long long spin_limit,
+                        cudaStream_t s) {
+    const int tbytes = dtype == GAI4_F32 ? 4 : 2;
+    Qmv4Plan p;
+    if (!plan_qmv4(N, K, gs, tbytes, &p)) return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int BR = (kCWarps / p.S) * p.R;
+    const int sbg = kItCols / gs;
+    const int n_it = (int)((K + kItCols - 1) / kItCols);
+    const bool box3 = K % kItCols == 0;
+    CUtensorMap wm, sm, bm;
+    if (box3) {
+        // [N][n_it][128 words] and [N][n_it][sbg] views; one box = one stage
+        const CUtensorMapDataType dt = tbytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+        cuuint64_t wd[3] = {(cuuint64_t)(kItCols / 8), (cuuint64_t)n_it, (cuuint64_t)N};
+        cuuint64_t wst[2] = {(cuuint64_t)(kItCols / 2), (cuuint64_t)(K / 2)};
+        cuuint32_t wbox[3] = {(cuuint32_t)(kItCols / 8), (cuuint32_t)p.S, (cuuint32_t)BR};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(w), wd, wst, wbox, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        cuuint64_t sd[3] = {(cuuint64_t)sbg, (cuuint64_t)n_it, (cuuint64_t)N};
+        cuuint64_t sst[2] = {(cuuint64_t)(sbg * tbytes), (cuuint64_t)((K / gs) * tbytes)};
+        cuuint32_t sbox[3] = {(cuuint32_t)sbg, (cuuint32_t)p.S, (cuuint32_t)BR};
+        if (enc(&sm, dt, 3, const_cast<void*>(scales), sd, sst, sbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (enc(&bm, dt, 3, const_cast<void*>(biases), sd, sst, sbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        cuuint32_t box[2] = {(cuuint32_t)(kItCols / 8), (cuuint32_t)BR};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / gs), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)((K / gs) * tbytes)};
+        cuuint32_t box[2] = {(cuuint32_t)sbg, (cuuint32_t)BR};
+        cuuint32_t es[2] = {1, 1};
+        const CUtensorMapDataType dt = tbytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+        if (enc(&sm, dt, 2, const_cast<void*>(scales), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (enc(&bm, dt, 2, const_cast<void*>(biases), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    }
+    Qmv4Args a;
+    a.x = x;
+    a.out = out;
+    a.N = N;
+    a.K = K;
+    int lg = 0;
+    while ((1 << lg) < gs) ++lg;
+    a.gs_log2 = lg;
+    a.S = p.S;
+    a.n_it = (int)((K + kItCols - 1) / kItCols);
+    a.n_st = (a.n_it + p.S - 1) / p.S;
+    a.depth = p.depth;
+    a.n_blocks = p.n_blocks;
+    a.sbg = sbg;
+    a.w_slice = p.w_slice;
+    a.sb_slice = p.sb_slice;
+    a.stage_bytes = p.stage_bytes;
+    a.box3 = box3 ? 1 : 0;
+    a.flush = p.flush;
+    if (box3) {   // [row][iteration][...]
+        a.w_rs = (uint32_t)p.S * 512u;
+        a.w_is = 512u;
+        a.sb_rs = (uint32_t)(p.S * sbg);
+        a.sb_is = (uint32_t)sbg;
+    } else {      // [iteration][row][...]
+        a.w_rs = 512u;
+        a.w_is = p.w_slice;
+        a.sb_rs = (uint32_t)sbg;
+        a.sb_is = p.sb_slice / (uint32_t)tbytes;
+    }
+    a.mask_lo = kMaskLo;
+    a.mask_hi = kMaskHi;
+    a.one = kOne;
+    a.status = status;
+    a.spin_limit = spin_limit;
+    switch (dtype) {
+    case GAI4_F16: return launch_r<F16>(wm, sm, bm, a, p.R, p.smem, s);
+    case GAI4_F32: return launch_r<F32>(wm, sm, bm, a, p.R, p.smem, s);
+    default: return launch_r<BF16>(wm, sm, bm, a, p.R, p.smem, s);
+    }
+}
+
+}  // namespace gai4

@@ -116,6 +116,23 @@ def test_qmm_small_m_widths(bits, gs, M):
     assert_within(to_host_f64(out, "bf16"), ref, absdot, "bf16", f"qmm_t bits={bits} gs={gs} M={M}")
 
 
+# 4-bit shapes on the prefetching qmv kernel (scale rows a multiple of 16 bytes,
+# K >= 1024): K a multiple of 1024 takes one 3-D copy per stage, other K one
+# 2-D copy per 1024-column iteration with a ragged last iteration
+QMV4_SHAPES = [(1, 1024), (33, 1536), (300, 2560), (4099, 3072), (77, 5632), (1000, 2048)]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("gs", [32, 64, 128])
+@pytest.mark.parametrize("N,K", QMV4_SHAPES)
+def test_qmv_4bit_copy_layouts(N, K, gs, dtype):
+    _, packed, s, b, x = affine_problem(N, K, 1, 4, gs, dtype, seed=N + K + gs)
+    ref, absdot = oracle.qmm(packed, s, b, x[0], 4, gs, dtype)
+    got = _run_qmv(packed, s, b, x, 4, gs, dtype)
+    assert_within(got, ref, absdot, dtype, f"qmv N={N} K={K} gs={gs} {dtype}")
+    assert np.all(np.isfinite(got))
+
+
 def test_qmm_m1_equals_qmv():
     """qmm_t at M = 1 runs the qmv kernel: identical bits."""
     _, packed, s, b, x = affine_problem(300, 2048, 1, 4, 64, "bf16", seed=5)
