@@ -79,6 +79,20 @@ __device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t 
     return d;
 }
 
+#ifndef QMV4_PACKED_FMA
+#define QMV4_PACKED_FMA 1
+#endif
+
+// (acc.x + a_lo * b_lo, acc.y + a_hi * b_hi): two binary32 fmas in one instruction
+__device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo, float b_hi, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
 
 template <typename T, int R>
@@ -237,12 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&empty[slot]);
 
                 const float4 cst = cs[it * 32 + lane];
-                float ae[R], ao[R];
+                float2 acc[R];   // (even codes, odd codes)
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    ae[r] = cst.x;
-                    ao[r] = cst.y;
-                }
+                for (int r = 0; r < R; ++r) acc[r] = make_float2(cst.x, cst.y);
 #pragma unroll
                 for (int tw = 0; tw < 4; ++tw) {
                     const float4 p0 = xs[(it * 8 + 2 * tw) * 32 + lane];
@@ -250,23 +261,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
-                        uint32_t u = w << 15;   // codes 0, 1
-                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p0.x, ae[r]);
-                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p0.y, ao[r]);
-                        u = w << 7;             // codes 2, 3
-                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p0.z, ae[r]);
-                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p0.w, ao[r]);
-                        u = w >> 1;             // codes 4, 5
-                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p1.x, ae[r]);
-                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p1.y, ao[r]);
-                        u = w >> 9;             // codes 6, 7
-                        ae[r] = fmaf(__uint_as_float(lop3_andor(u, mlo, one)), p1.z, ae[r]);
-                        ao[r] = fmaf(__uint_as_float(lop3_andor(u, mhi, one)), p1.w, ao[r]);
+                        const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;   // codes (0,1) .. (6,7)
+                        if constexpr (QMV4_PACKED_FMA) {
+                            acc[r] = ffma2(lop3_andor(u0, mlo, one), lop3_andor(u0, mhi, one), p0.x, p0.y, acc[r]);
+                            acc[r] = ffma2(lop3_andor(u1, mlo, one), lop3_andor(u1, mhi, one), p0.z, p0.w, acc[r]);
+                            acc[r] = ffma2(lop3_andor(u2, mlo, one), lop3_andor(u2, mhi, one), p1.x, p1.y, acc[r]);
+                            acc[r] = ffma2(lop3_andor(u3, mlo, one), lop3_andor(u3, mhi, one), p1.z, p1.w, acc[r]);
+                        } else {
+                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u0, mlo, one)), p0.x, acc[r].x);
+                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u0, mhi, one)), p0.y, acc[r].y);
+                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u1, mlo, one)), p0.z, acc[r].x);
+                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u1, mhi, one)), p0.w, acc[r].y);
+                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u2, mlo, one)), p1.x, acc[r].x);
+                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u2, mhi, one)), p1.y, acc[r].y);
+                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u3, mlo, one)), p1.z, acc[r].x);
+                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u3, mhi, one)), p1.w, acc[r].y);
+                        }
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float qx = fmaf(256.f, ae[r], 16.f * ao[r]);   // sum q x of the chunk
+                    const float qx = fmaf(256.f, acc[r].x, 16.f * acc[r].y);   // sum q x of the chunk
                     part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.z, part[r]));
                 }
             } else {
