@@ -7,7 +7,7 @@
 // reduction.)
 //
 // GB300 design:
-//  * One CTA per SM, persistent over blocks of BR = (16 / S) * R rows: 16
+//  * One CTA per SM, persistent over blocks of BR = (24 / S) * R rows: 24
 //    consumer warps and one producer warp. A consumer warp owns R rows of a
 //    block; S warps split the 1024-column iterations of a row group when rows
 //    alone would leave SMs idle. A lane owns 32 consecutive codes (16 bytes)
@@ -41,7 +41,10 @@ namespace {
 
 using namespace pipe;
 
-constexpr int kCWarps = 16;                        // consumer warps
+#ifndef QMV4_CWARPS
+#define QMV4_CWARPS 24
+#endif
+constexpr int kCWarps = QMV4_CWARPS;               // consumer warps
 constexpr int kThreads = 32 * (kCWarps + 1);       // + one producer warp
 constexpr int kItCols = 1024;                      // columns of one warp iteration (32 lanes x 32 codes)
 constexpr int kMaxDepth = 8;
@@ -174,47 +177,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- consumers: stage x once ----------------
+    // a thread takes 8 consecutive elements (a quarter of a 32-element chunk);
+    // the 4 quarters of a chunk sit in 4 adjacent lanes and add their sums
+    // with shuffles
     const St* xg = static_cast<const St*>(a.x);
     const int64_t K = a.K;
-    for (int c = threadIdx.x; c < n_it * 32; c += kCWarps * 32) {
-        float v[32];
-        const int64_t k0 = (int64_t)c * 32;
+    for (int u = threadIdx.x; u < n_it * 128; u += kCWarps * 32) {   // n_it * 128 is a multiple of 32
+        const int c = u >> 2, qq = u & 3;
+        const int64_t k0 = (int64_t)u * 8;
+        float v[8];
         if (k0 < K) {   // K is a multiple of 32: a chunk is all in or all out
             if constexpr (T::kBytes == 4) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 f = *reinterpret_cast<const float4*>(xg + k0 + 4 * j);
-                    v[4 * j] = f.x;
-                    v[4 * j + 1] = f.y;
-                    v[4 * j + 2] = f.z;
-                    v[4 * j + 3] = f.w;
-                }
+                const float4 f0 = *reinterpret_cast<const float4*>(xg + k0);
+                const float4 f1 = *reinterpret_cast<const float4*>(xg + k0 + 4);
+                v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+                v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
             } else {
+                const uint4 q = *reinterpret_cast<const uint4*>(xg + k0);
+                const uint32_t uu[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(xg + k0 + 8 * j);
-                    const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        v[8 * j + 2 * h] = T::to_f32((uint16_t)(uu[h] & 0xFFFFu));
-                        v[8 * j + 2 * h + 1] = T::to_f32((uint16_t)(uu[h] >> 16));
-                    }
+                for (int h = 0; h < 4; ++h) {
+                    v[2 * h] = T::to_f32((uint16_t)(uu[h] & 0xFFFFu));
+                    v[2 * h + 1] = T::to_f32((uint16_t)(uu[h] >> 16));
                 }
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            for (int j = 0; j < 8; ++j) v[j] = 0.f;
         }
-        float xe = 0.f, xo = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            xe += v[2 * j];
-            xo += v[2 * j + 1];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            xs[((c >> 5) * 8 + j) * 32 + (c & 31)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        cs[c] = make_float4(-xe, -xo, xe + xo, 0.f);
+        xs[((c >> 5) * 8 + 2 * qq) * 32 + (c & 31)] = make_float4(v[0], v[1], v[2], v[3]);
+        xs[((c >> 5) * 8 + 2 * qq + 1) * 32 + (c & 31)] = make_float4(v[4], v[5], v[6], v[7]);
+        // chunk sums in a fixed order: quarters (0 + 1) + (2 + 3)
+        float xe = (v[0] + v[2]) + (v[4] + v[6]);
+        float xo = (v[1] + v[3]) + (v[5] + v[7]);
+        xe += __shfl_xor_sync(0xffffffffu, xe, 1);
+        xo += __shfl_xor_sync(0xffffffffu, xo, 1);
+        xe += __shfl_xor_sync(0xffffffffu, xe, 2);
+        xo += __shfl_xor_sync(0xffffffffu, xo, 2);
+        if (qq == 0) cs[c] = make_float4(-xe, -xo, xe + xo, 0.f);
     }
     consumer_bar();
 
@@ -341,7 +341,8 @@ bool plan_qmv4(int64_t N, int64_t K, int gs, int tbytes, Qmv4Plan* out) {
     bool found = false;
     int64_t best = 0;
     for (int R : {4, 2, 1}) {
-        for (int S : {1, 2, 4, 8, 16}) {
+        for (int S : {1, 2, 3, 4, 6, 8, 12, 16, 24}) {
+            if (kCWarps % S != 0) continue;
             const int BR = (kCWarps / S) * R;
             const uint32_t w_slice = (uint32_t)BR * 512;
             const uint32_t sb_slice = ((uint32_t)BR * sbg * tbytes + 127) / 128 * 128;
