@@ -332,6 +332,8 @@ struct Params {
     int a_stages;
     int n_issuers;        // MMA issuer warps = accumulators (1 or 2)
     int sb_boxes;         // 8-group boxes per stage and tensor reserved in shared memory (1 or 2)
+    uint32_t nib_mask;    // 0x000F000F
+    uint32_t magic;       // bit pattern of C (128 for bf16, 1024 for f16) in both halves
     int* status;
     long long spin_limit;
 };
@@ -359,13 +361,23 @@ __device__ __forceinline__ void piece_of(const SplitPlan& pl, int64_t K, int p, 
 // 4-bit codes: one 32-bit word (8 codes, low nibble first) -> 4 registers of
 // w_hat pairs (k, k+1) in 16-bit format T.
 // ---------------------------------------------------------------------------
+// (a & b) | c as one three-input logic instruction (b, c in registers: a
+// logic op takes at most one immediate operand)
+__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// nib_mask = 0x000F000F and magic = C in both halves, passed in registers
 template <bool BF>
-__device__ __forceinline__ void dequant_word4(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* o) {
+__device__ __forceinline__ void dequant_word4(uint32_t w, uint32_t s2, uint32_t b2, uint32_t nib_mask,
+                                              uint32_t magic, uint32_t* o) {
     constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;   // 128.0 / 1024.0 in both halves
     uint32_t r[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t p = ((w >> (4 * j)) & 0x000F000Fu) | kMagic;   // (C + q_j, C + q_{j+4})
+        const uint32_t p = lop3_andor(w >> (4 * j), nib_mask, magic);  // (C + q_j, C + q_{j+4})
         const uint32_t q = hsub2<BF>(p, kMagic);                       // (q_j, q_{j+4}) exact
         r[j] = hfma2<BF>(q, s2, b2);                                   // (w_j, w_{j+4})
     }
@@ -391,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (128-byte swizzle atoms)
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // pointer arithmetic on the shared array keeps accesses in the shared state space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int mt = p.mt;
     const int XS = p.x_stages, WS = p.w_stages, AS = p.a_stages;
@@ -562,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t* brow = p.biases + (row_ok ? row : 0) * p.groups;
         const uint8_t* wrow = wbuf + (size_t)r * 128;
         const int lg = p.gs_log2;
+        const uint32_t nibm = p.nib_mask, magic = p.magic;
 
         // scale / bias of the two 32-column halves of this thread's 64 columns
         // (a half lies in one group), read from global memory two stages
@@ -630,14 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t o[32];
                 const uint32_t s2a = sc[0] | (sc[0] << 16), b2a = bc[0] | (bc[0] << 16);
                 const uint32_t s2b = sc[1] | (sc[1] << 16), b2b = bc[1] | (bc[1] << 16);
-                dequant_word4<BF>(va.x, s2a, b2a, &o[0]);
-                dequant_word4<BF>(va.y, s2a, b2a, &o[4]);
-                dequant_word4<BF>(va.z, s2a, b2a, &o[8]);
-                dequant_word4<BF>(va.w, s2a, b2a, &o[12]);
-                dequant_word4<BF>(vb.x, s2b, b2b, &o[16]);
-                dequant_word4<BF>(vb.y, s2b, b2b, &o[20]);
-                dequant_word4<BF>(vb.z, s2b, b2b, &o[24]);
-                dequant_word4<BF>(vb.w, s2b, b2b, &o[28]);
+                dequant_word4<BF>(va.x, s2a, b2a, nibm, magic, &o[0]);
+                dequant_word4<BF>(va.y, s2a, b2a, nibm, magic, &o[4]);
+                dequant_word4<BF>(va.z, s2a, b2a, nibm, magic, &o[8]);
+                dequant_word4<BF>(va.w, s2a, b2a, nibm, magic, &o[12]);
+                dequant_word4<BF>(vb.x, s2b, b2b, nibm, magic, &o[16]);
+                dequant_word4<BF>(vb.y, s2b, b2b, nibm, magic, &o[20]);
+                dequant_word4<BF>(vb.z, s2b, b2b, nibm, magic, &o[24]);
+                dequant_word4<BF>(vb.w, s2b, b2b, nibm, magic, &o[28]);
                 tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)part * 32u, o);
             }
             tmem_st_wait();
@@ -835,6 +849,8 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.a_stages = as;
     p.n_issuers = ni;
     p.sb_boxes = sb_boxes > 0 ? sb_boxes : 1;
+    p.nib_mask = 0x000F000Fu;
+    p.magic = L.is_bf16 ? 0x43004300u : 0x64006400u;
     p.status = L.status;
     p.spin_limit = L.spin_limit;
 
