@@ -47,8 +47,14 @@ QMM_SHAPES = [(2048, 2048, 22), (4096, 4096, 16), (10752, 2048, 85), (14336, 409
 BLOCKQ_SHAPES = [(4096, 4096), (14336, 5120)]                                              # (N, K)
 BITS, GS = 4, 64
 
+# sources whose kernels run in each family's calls (a recorded ncu traffic
+# figure is used only while these files are unchanged)
+_CSRC = "gemm_affine_int4_gb300/csrc/"
 KERNEL_SOURCES = {
-    "qmv": ["gemm_affine_int4_gb300/csrc/affine_gemv.cuh", "gemm_affine_int4_gb300/csrc/common.cuh"],
+    "qmv": [_CSRC + f for f in ("qmv4.cu", "pipeline.cuh", "common.cuh", "api.cu")],
+    "qmm_t": [_CSRC + f for f in ("qmm_tc.cu", "pipeline.cuh", "common.cuh", "api.cu")],
+    "q8_0": [_CSRC + f for f in ("blockq.cu", "common.cuh", "api.cu")],
+    "q4_k": [_CSRC + f for f in ("blockq.cu", "common.cuh", "api.cu")],
 }
 
 

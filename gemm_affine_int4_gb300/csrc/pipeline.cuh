@@ -35,6 +35,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+#ifndef GAI4_WAIT_HINT
+#define GAI4_WAIT_HINT 1
+#endif
+
+// try_wait that may suspend the thread until the phase completes (or about
+// `ns` nanoseconds pass): a waiting warp then issues almost no instructions
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 struct Ctl {
     int* status;            // device status word
     long long limit;        // clock64 cycles a single wait may take
@@ -45,7 +61,7 @@ struct Ctl {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!(GAI4_WAIT_HINT ? mbar_try_wait_hint(bar, parity, 0x10000u) : mbar_try_wait(bar, parity))) {
         if (*c.abort_) return false;
         if (clock64() - t0 > c.limit) {
             *c.abort_ = 1;
