@@ -207,7 +207,7 @@ using namespace pipe;
 constexpr int kTileN = 128;      // weight rows per CTA (MMA M)
 constexpr int kBK = 256;         // K columns per weight / A stage
 constexpr int kXBK = 128;        // K columns per activation stage (two 64-column swizzle atoms)
-constexpr int kMaxWStages = 8;   // packed-weight ring (runtime depth <= this)
+constexpr int kMaxWStages = 12;  // packed-weight ring (runtime depth <= this)
 constexpr int kMaxAStages = 3;   // tensor-memory A ring (128 columns each; runtime depth <= this)
 constexpr int kMaxXStages = 8;   // activation ring (runtime depth <= this)
 constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
@@ -267,26 +267,12 @@ __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
         : "memory");
 }
 
-// 32 consecutive 32-bit columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
 }
-// 16 consecutive 32-bit columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
@@ -641,18 +627,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(&a_empty[sa], (uint32_t)(pa ^ 1), ctl)) break;
             fence_after();
             if (active) {
-                uint32_t o[32];
                 const uint32_t s2a = sc[0] | (sc[0] << 16), b2a = bc[0] | (bc[0] << 16);
                 const uint32_t s2b = sc[1] | (sc[1] << 16), b2b = bc[1] | (bc[1] << 16);
-                dequant_word4<BF>(va.x, s2a, b2a, nibm, magic, &o[0]);
-                dequant_word4<BF>(va.y, s2a, b2a, nibm, magic, &o[4]);
-                dequant_word4<BF>(va.z, s2a, b2a, nibm, magic, &o[8]);
-                dequant_word4<BF>(va.w, s2a, b2a, nibm, magic, &o[12]);
-                dequant_word4<BF>(vb.x, s2b, b2b, nibm, magic, &o[16]);
-                dequant_word4<BF>(vb.y, s2b, b2b, nibm, magic, &o[20]);
-                dequant_word4<BF>(vb.z, s2b, b2b, nibm, magic, &o[24]);
-                dequant_word4<BF>(vb.w, s2b, b2b, nibm, magic, &o[28]);
-                tmem_st32(tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)part * 32u, o);
+                const uint32_t ta = tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)part * 32u;
+                // one 8-column store per word pair
+                const uint32_t wds[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                    uint32_t o8[8];
+                    const uint32_t s2 = pr < 2 ? s2a : s2b, b2 = pr < 2 ? b2a : b2b;
+                    dequant_word4<BF>(wds[2 * pr], s2, b2, nibm, magic, &o8[0]);
+                    dequant_word4<BF>(wds[2 * pr + 1], s2, b2, nibm, magic, &o8[4]);
+                    tmem_st8(ta + (uint32_t)pr * 8u, o8);
+                }
             }
             tmem_st_wait();
             fence_before();
@@ -814,18 +801,26 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
                 if (((j * KU / st) * L.plan.unit) % 256 != 0) aligned = false;
         sb_boxes = aligned ? 1 : 2;
     }
-    // Activation ring as deep as possible (up to 8) while it leaves four
-    // weight stages: activation tiles are re-read by every CTA from L2 and
-    // their latency needs the lookahead.
+    // The weight ring gets the shared memory first: its stages stream from
+    // DRAM and the bytes in flight per SM set the bandwidth (about 7 stages
+    // of 16 KB are needed); activation tiles are L2 hits and need only a
+    // short ring (at least 3 stages, 2 for the widest tiles).
     const size_t kBars = 512;
     const size_t x_stage = (size_t)mt * tc::kXBK * 2;
     const size_t w_stage = (size_t)kTileN * kBK / 2 + 2u * tc::kSbBox * (size_t)sb_boxes;
     const size_t budget = 224 * 1024 - 1024 - kBars;
-    int xs = (int)((budget - 4 * w_stage) / x_stage);
-    xs = xs < 2 ? 2 : (xs > kMaxXStages ? kMaxXStages : xs);
-    const size_t x_bytes = (size_t)xs * x_stage;
-    int ws = (int)((budget - x_bytes) / w_stage);
+    // With two issuers taking alternate activation stages the ring depth must
+    // be even: then every slot is always consumed by the same issuer, in order.
+    // (With an odd depth a slot passes between issuers, and an issuer more than
+    // a ring ahead of the other could wait on the parity of a phase that has
+    // not started, which mbarrier.try_wait.parity reports as complete.)
+    const int xs_min = mt > 128 ? 2 : (ni == 2 ? 4 : 3);
+    int ws = (int)((budget - (size_t)xs_min * x_stage) / w_stage);
     ws = ws < 3 ? 3 : (ws > kMaxWStages ? kMaxWStages : ws);
+    int xs = (int)((budget - (size_t)ws * w_stage) / x_stage);
+    xs = xs < 2 ? 2 : (xs > kMaxXStages ? kMaxXStages : xs);
+    if (ni == 2) xs &= ~1;
+    const size_t x_bytes = (size_t)xs * x_stage;
     size_t smem = 1024 + x_bytes + (size_t)ws * w_stage + kBars;
     if (smem < 120 * 1024) smem = 120 * 1024;
     static_assert((2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxAStages + 1) * 8 + 8 <= 512, "barrier area");
@@ -847,6 +842,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.x_stages = xs;
     p.w_stages = ws;
     p.a_stages = as;
+    if (ni == 2 && (xs & 1)) return cudaErrorInvalidValue;   // slot ownership invariant above
     p.n_issuers = ni;
     p.sb_boxes = sb_boxes > 0 ? sb_boxes : 1;
     p.nib_mask = 0x000F000Fu;
@@ -854,12 +850,15 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.status = L.status;
     p.spin_limit = L.spin_limit;
 
-    auto kern = L.is_bf16 ? (sbt ? tc::qmm_tc4_kernel<true, true> : tc::qmm_tc4_kernel<true, false>)
-                          : (sbt ? tc::qmm_tc4_kernel<false, true> : tc::qmm_tc4_kernel<false, false>);
+    using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const tc::Params);
+    static const KernFn kernels[4] = {tc::qmm_tc4_kernel<false, false>, tc::qmm_tc4_kernel<true, false>,
+                                      tc::qmm_tc4_kernel<false, true>, tc::qmm_tc4_kernel<true, true>};
+    const int which = (L.is_bf16 ? 1 : 0) + (sbt ? 2 : 0);
+    const KernFn kern = kernels[which];
     static unsigned long long configured[4] = {0ull, 0ull, 0ull, 0ull};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int which = (L.is_bf16 ? 1 : 0) + (sbt ? 2 : 0);
     if (dev >= 64 || !(configured[which] & (1ull << dev))) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
