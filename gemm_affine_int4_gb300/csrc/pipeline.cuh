@@ -15,6 +15,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// A loop-invariant operand held in a register for the whole loop. Values that
+// come from kernel parameters are otherwise re-read from the constant bank
+// with one move instruction per use (a logic op takes at most one such
+// operand); a warp shuffle result cannot be re-derived that way. The calling
+// warp must be converged.
+__device__ __forceinline__ uint32_t pin_reg(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }

@@ -205,15 +205,17 @@ namespace tc {
 using namespace pipe;
 
 constexpr int kTileN = 128;      // weight rows per CTA (MMA M)
-constexpr int kBK = 256;         // K columns per weight / A stage
-constexpr int kXBK = 128;        // K columns per activation stage (two 64-column swizzle atoms)
-constexpr int kMaxWStages = 12;  // packed-weight ring (runtime depth <= this)
-constexpr int kMaxAStages = 3;   // tensor-memory A ring (128 columns each; runtime depth <= this)
+constexpr int kBK = 256;         // K columns per weight stage
+constexpr int kAK = 128;         // K columns per A stage = per activation stage
+constexpr int kXBK = kAK;        // (two 64-column swizzle atoms)
+constexpr uint32_t kAStageCols = kAK / 2;   // tensor-memory columns of one A stage (bf16 pairs)
+constexpr int kMaxWStages = 12;  // packed-weight ring (runtime depth <= this, even)
+constexpr int kMaxAStages = 8;   // tensor-memory A ring (runtime depth 4..8)
 constexpr int kMaxXStages = 8;   // activation ring (runtime depth <= this)
 constexpr int kMaxMt = 256;      // x rows per CTA (MMA N <= 256)
 constexpr int kTmemCols = 512;   // one CTA per SM owns all of tensor memory
 constexpr int kMaxIssuers = 2;   // MMA issuer warps (2 and 3), one accumulator each
-constexpr int kDequantWarps = 16;   // 4 per tensor-memory lane quadrant, 64 columns each
+constexpr int kDequantWarps = 16;   // 4 groups of 4 (one warp per tensor-memory lane quadrant)
 constexpr int kDequantWarp0 = 4;
 constexpr int kThreads = 32 * (kDequantWarp0 + kDequantWarps);
 constexpr uint32_t kSbBox = 8 * kTileN * 2;    // one TMA box of scales or biases: 8 groups x 128 rows, u16
@@ -225,10 +227,10 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 // start address >> 4, leading byte offset (unused for this layout) = 1,
 // stride byte offset = 1024 (8 rows x 128 B), descriptor version 1, layout
 // SWIZZLE_128B (2).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
+// Low word: start address and leading byte offset; high word: stride byte
+// offset, version and layout (the same for every operand of this kernel).
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
 
 // instruction descriptor, kind::f16: fp32 accumulate, A/B bf16 (1) or f16 (0),
 // both K-major, N = mt, M = 128
@@ -237,27 +239,16 @@ __host__ __device__ constexpr uint32_t make_idesc(int is_bf16, int mt) {
            ((uint32_t)(kTileN >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-// the same two operations executed by a converged warp: one elected lane issues
-__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// the same two operations executed by a converged warp: one elected lane
+// issues; the activation descriptor is given by its low word (the high word is
+// kSw128DescHi)
+__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_desc_lo,
                                                     uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n .reg .pred p, e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p, e;\n .reg .b32 r;\n .reg .b64 d;\n elect.sync r|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " mov.b64 d, {%2, %5};\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], d, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_desc_lo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
@@ -282,6 +273,22 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
                  : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// loads addressed in the shared state space (32-bit addresses); volatile with a
+// memory clobber so that they stay after the mbarrier wait that publishes the data
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return (uint32_t)v;
+}
 
 // packed 16-bit pair arithmetic (one rounding per result)
 template <bool BF>
@@ -420,19 +427,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nk64 = (int)((k_end - k_begin) / 64);            // 64-column units in this piece
     const int nst = (nk64 + 3) / 4;                            // 256-column weight / A stages
     const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
+    const int nas = nxs;                                       // = A stages
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < WS; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], kDequantWarps);   // one arrive per dequantize warp
+            mbar_init(&w_empty[i], 8);   // both halves: one arrive per warp of two groups
         }
         for (int i = 0; i < XS; ++i) {
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 1);               // tcgen05.commit
         }
         for (int i = 0; i < AS; ++i) {
-            mbar_init(&a_full[i], kDequantWarps);
-            mbar_init(&a_empty[i], p.n_issuers);   // one commit per issuer
+            mbar_init(&a_full[i], 4);              // the 4 warps of one group
+            mbar_init(&a_empty[i], 1);             // the commit of the stage's issuer
         }
         mbar_init(acc_full, p.n_issuers);         // one commit per issuer
         *abort_flag = 0;
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t acc_col = 0;   // accumulator of issuer j: columns [j * mt, (j + 1) * mt)
     const int NI = p.n_issuers;
-    const uint32_t a_col0 = (uint32_t)kTmemCols - 128u * (uint32_t)AS;   // A ring at the top
+    const uint32_t a_col0 = (uint32_t)kTmemCols - kAStageCols * (uint32_t)AS;   // A ring at the top
     Ctl ctl{p.status, p.spin_limit, abort_flag};
 
     if (warp == 0) {
@@ -500,46 +508,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2 || warp == 3) {
         // ---------------- MMA issuers (whole warps) ----------------
+        // issuer jw takes the A stages i == jw (mod NI), each with its
+        // activation stage i, into its own accumulator
         const int jw = warp - 2;
         if (jw < NI) {
             const uint32_t idesc = make_idesc(BF ? 1 : 0, mt);
             const uint32_t acc_tm = tmem_base + acc_col + (uint32_t)(jw * mt);
             uint32_t acc_flag = 0;
-            const int hh0 = NI == 2 ? jw : 0, hh1 = NI == 2 ? jw + 1 : 2;
-            int sa = 0, pa = 0;
-            const int xstep = hh1 - hh0 == 1 ? 2 : 1;   // activation stages between this issuer's consecutive ones
-            int sx = hh0, px = 0;                       // slot / parity of this issuer's next activation stage
-            for (int i = 0; i < nst; ++i) {
+            const uint32_t xs_base = smem_u32(xbuf);
+            const uint32_t atom_step = (uint32_t)mt * 8u;   // one 64-column swizzle atom (mt x 128 B) >> 4
+            const uint32_t a_tm0 = tmem_base + a_col0;
+            int sa = jw, pa = 0, sx = jw, px = 0;   // slots / parities of stage i (both rings have even depth with two issuers)
+            for (int i = jw; i < nas; i += NI) {
                 if (!warp_wait(&a_full[sa], (uint32_t)pa, ctl)) break;
-                bool ok = true;
-                for (int hh = hh0; hh < hh1; ++hh) {    // this issuer's activation stage(s) of this A stage
-                    const int j = 2 * i + hh;
-                    if (j >= nxs) break;
-                    if (!warp_wait(&x_full[sx], (uint32_t)px, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                    const int kk_end = (2 * j + 1 < nk64) ? 8 : 4;   // a stage may end with one 64-column unit
-                    const uint32_t xaddr = smem_u32(xbuf + (size_t)sx * x_stage_bytes);
-                    const uint32_t a_t0 = tmem_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)hh * 64u;
-                    for (int kk = 0; kk < kk_end; ++kk) {
-                        const uint32_t baddr =
-                            xaddr + (uint32_t)(kk >> 2) * (uint32_t)mt * 128u + (uint32_t)(kk & 3) * 32u;
-                        mma_f16_tmem_a_warp(acc_tm, a_t0 + (uint32_t)kk * 8u, sw128_desc(baddr), idesc, acc_flag);
+                if (!warp_wait(&x_full[sx], (uint32_t)px, ctl)) break;
+                fence_after();
+                const int kk_end = (2 * i + 1 < nk64) ? 8 : 4;   // the last stage may hold one 64-column unit
+                // descriptor of the stage's first 16 columns; the next ones
+                // advance the 14-bit start-address field (no carry: shared
+                // addresses are below 2^18)
+                const uint32_t d0 = sw128_desc_lo(xs_base + (uint32_t)sx * x_stage_bytes);
+                const uint32_t a_t0 = a_tm0 + (uint32_t)sa * kAStageCols;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    if (kk < kk_end) {
+                        mma_f16_tmem_a_warp(acc_tm, a_t0 + (uint32_t)kk * 8u,
+                                            d0 + (uint32_t)(kk >> 2) * atom_step + (uint32_t)(kk & 3) * 2u, idesc,
+                                            acc_flag);
                         acc_flag = 1;
                     }
-                    mma_commit_warp(&x_empty[sx]);
-                    sx += xstep;
-                    if (sx >= XS) {
-                        sx -= XS;
-                        px ^= 1;
-                    }
                 }
-                if (!ok) break;
+                mma_commit_warp(&x_empty[sx]);
                 mma_commit_warp(&a_empty[sa]);
-                if (++sa == AS) {
-                    sa = 0;
+                sx += NI;
+                if (sx >= XS) {
+                    sx -= XS;
+                    px ^= 1;
+                }
+                sa += NI;
+                if (sa >= AS) {
+                    sa -= AS;
                     pa ^= 1;
                 }
             }
@@ -550,107 +558,130 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- dequantize, then epilogue ----------------
+        // Warp group grp (4 warps, one per tensor-memory lane quadrant) takes
+        // the A stages i == grp (mod 4): 128 columns, i.e. the half (i & 1) =
+        // (grp & 1) of weight stage i / 2, for the 32 rows of its quadrant.
         const int dw = warp - kDequantWarp0;        // 0..15
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
-        const int part = dw >> 2;                   // which 64 of the stage's 256 columns
+        const int grp = dw >> 2;
+        const int hw = grp & 1;                     // half of every weight stage this group reads
         const int r = quad * 32 + lane;             // weight row within the tile
         const int64_t row = n0 + r;
         const bool row_ok = row < p.N;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int lg = p.gs_log2;
+        const uint32_t nibm = pin_reg(p.nib_mask), magic = pin_reg(p.magic);
+        // shared addresses of this thread's four 16-byte chunks (4 hw .. 4 hw + 3)
+        // of its row in ring slot 0: 128-byte rows, 128-byte TMA swizzle
+        // (16-byte chunk c of row r at chunk c ^ (r & 7))
+        const uint32_t wrow_s = smem_u32(wbuf) + (uint32_t)r * 128u;
+        uint32_t wc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wc[c] = wrow_s + 16u * (uint32_t)((4 * hw + c) ^ (r & 7));
+        const uint32_t ta0 = tmem_base + lane_base + a_col0;
+        // TMA-staged scales / biases: row r of each 8-group box, in slot 0
+        const uint32_t sb0 = smem_u32(sbbuf) + (uint32_t)r * 16u;
+        const uint32_t bias_off = (uint32_t)p.sb_boxes * kSbBox;
+        // group offsets of the four 32-column quarters within the weight
+        // stage; every piece starts on a group boundary and gs divides the
+        // 256-column stage
+        int cq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cq[q] = (128 * hw + 32 * q) >> lg;
+        const int gstep2 = 2 * (kBK >> lg);
+        int g = (int)(k_begin >> lg) + (grp >> 1) * (kBK >> lg);   // first group of weight stage i / 2
+
         const uint16_t* srow = p.scales + (row_ok ? row : 0) * p.groups;
         const uint16_t* brow = p.biases + (row_ok ? row : 0) * p.groups;
-        const uint8_t* wrow = wbuf + (size_t)r * 128;
-        const int lg = p.gs_log2;
-        const uint32_t nibm = p.nib_mask, magic = p.magic;
-
-        // scale / bias of the two 32-column halves of this thread's 64 columns
-        // (a half lies in one group), read from global memory two stages
-        // ahead when they do not come by TMA
-        auto load_sb = [&](int i, uint32_t (&sv)[2], uint32_t (&bv)[2]) {
+        // scale / bias of the four quarters of A stage i, from global memory
+        // (when they do not come by TMA), one of this group's stages ahead
+        auto load_sb = [&](int i, uint32_t (&sv)[4], uint32_t (&bv)[4]) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                sv[h] = 0u;
-                bv[h] = 0u;
-                if (i < nst && 4 * i + part < nk64 && row_ok) {
-                    const int64_t g = (k_begin + (int64_t)kBK * i + 64 * part + 32 * h) >> lg;
-                    sv[h] = __ldg(srow + g);
-                    bv[h] = __ldg(brow + g);
+            for (int q = 0; q < 4; ++q) {
+                sv[q] = 0u;
+                bv[q] = 0u;
+                if (i < nas && 2 * i + (q >> 1) < nk64 && row_ok) {
+                    const int64_t gg = (k_begin + (int64_t)kAK * i + 32 * q) >> lg;
+                    sv[q] = __ldg(srow + gg);
+                    bv[q] = __ldg(brow + gg);
                 }
             }
         };
-        uint32_t s0[2] = {0u, 0u}, b0[2] = {0u, 0u}, s1[2] = {0u, 0u}, b1[2] = {0u, 0u};
-        if constexpr (!SBT) {
-            load_sb(0, s0, b0);
-            load_sb(1, s1, b1);
-        }
+        uint32_t s1[4] = {0u, 0u, 0u, 0u}, b1[4] = {0u, 0u, 0u, 0u};
+        if constexpr (!SBT) load_sb(grp, s1, b1);
 
-        int sw = 0, pw = 0, sa = 0, pa = 0;   // ring slots and phase parities of stage i
-        for (int i = 0; i < nst; ++i) {
-            const bool active = 4 * i + part < nk64;   // the last stage may hold fewer 64-column units
-            uint32_t sc[2], bc[2];
+        // weight stage v = i / 2 advances by 2 per iteration (even ring depth:
+        // this group always meets the same slots); A stage i advances by 4
+        int sw = grp >> 1, pw = 0, sa = grp, pa = 0;   // (WS >= 4, AS >= 4)
+        uint32_t w_off = (uint32_t)sw * w_stage_bytes, sb_off = (uint32_t)sw * sb_stage_bytes;
+        for (int i = grp; i < nas; i += 4) {
+            const bool hi_active = 2 * i + 1 < nk64;   // the last stage may hold one 64-column unit
+            uint32_t sc[4], bc[4];
             if constexpr (!SBT) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    sc[h] = s0[h];
-                    bc[h] = b0[h];
-                    s0[h] = s1[h];
-                    b0[h] = b1[h];
+                for (int q = 0; q < 4; ++q) {
+                    sc[q] = s1[q];
+                    bc[q] = b1[q];
                 }
-                load_sb(i + 2, s1, b1);
+                load_sb(i + 4, s1, b1);
             }
             if (!warp_wait(&w_full[sw], (uint32_t)pw, ctl)) break;
-            // this thread's 32 bytes (64 codes) of the row: 128-byte rows,
-            // 128-byte TMA swizzle (16-byte chunk c of row r at chunk c ^ (r & 7))
-            const uint8_t* rowp = wrow + (size_t)sw * w_stage_bytes;
-            const uint4 va = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * part) ^ (r & 7)));
-            const uint4 vb = *reinterpret_cast<const uint4*>(rowp + 16 * ((2 * part + 1) ^ (r & 7)));
-            if constexpr (SBT) {
-                const int64_t kst = k_begin + (int64_t)kBK * i;
-                int x0, nbox;
-                stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), lg, x0, nbox);
-                const uint8_t* sb = sbbuf + (size_t)sw * sb_stage_bytes;
+            uint4 v[4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // group of this half, relative to the box origin: box (idx >> 3), column (idx & 7)
-                    const int idx = active ? (int)((kst + 64 * part + 32 * h) >> lg) - x0 : 0;
-                    const uint32_t off = (uint32_t)(idx >> 3) * kSbBox + (uint32_t)r * 16u + 2u * (uint32_t)(idx & 7);
-                    sc[h] = *reinterpret_cast<const uint16_t*>(sb + off);
-                    bc[h] = *reinterpret_cast<const uint16_t*>(sb + (uint32_t)p.sb_boxes * kSbBox + off);
+            for (int c = 0; c < 4; ++c) v[c] = lds128(wc[c] + w_off);
+            if constexpr (SBT) {
+                // group of each quarter relative to the slot's first box origin
+                // (g rounded down to a multiple of 8): box (idx >> 3), column
+                // (idx & 7); a quarter past the piece reads column 0 (in bounds, unused)
+                const int rel = g & 7;
+                const uint32_t sbs = sb0 + sb_off;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int idx = (q < 2 || hi_active) ? rel + cq[q] : 0;
+                    const uint32_t o = (uint32_t)(idx >> 3) * kSbBox + 2u * (uint32_t)(idx & 7);
+                    sc[q] = lds16(sbs + o);
+                    bc[q] = lds16(sbs + bias_off + o);
                 }
             }
             // the stage is refilled by TMA (async proxy): order these generic
-            // reads before that write, then release the stage
+            // reads before that write, then release this half of the stage
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[sw]);
 
             if (!warp_wait(&a_empty[sa], (uint32_t)(pa ^ 1), ctl)) break;
             fence_after();
-            if (active) {
-                const uint32_t s2a = sc[0] | (sc[0] << 16), b2a = bc[0] | (bc[0] << 16);
-                const uint32_t s2b = sc[1] | (sc[1] << 16), b2b = bc[1] | (bc[1] << 16);
-                const uint32_t ta = tmem_base + lane_base + a_col0 + (uint32_t)sa * 128u + (uint32_t)part * 32u;
-                // one 8-column store per word pair
-                const uint32_t wds[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            const uint32_t ta = ta0 + (uint32_t)sa * kAStageCols;
+            // one 8-column store per word pair (a quarter past the piece is
+            // decoded from whatever the slot holds; its columns are not read)
 #pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    uint32_t o8[8];
-                    const uint32_t s2 = pr < 2 ? s2a : s2b, b2 = pr < 2 ? b2a : b2b;
-                    dequant_word4<BF>(wds[2 * pr], s2, b2, nibm, magic, &o8[0]);
-                    dequant_word4<BF>(wds[2 * pr + 1], s2, b2, nibm, magic, &o8[4]);
-                    tmem_st8(ta + (uint32_t)pr * 8u, o8);
-                }
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t s2 = __byte_perm(sc[c], 0u, 0x1010), b2 = __byte_perm(bc[c], 0u, 0x1010);
+                uint32_t o8[8];
+                dequant_word4<BF>(v[c].x, s2, b2, nibm, magic, &o8[0]);
+                dequant_word4<BF>(v[c].y, s2, b2, nibm, magic, &o8[4]);
+                tmem_st8(ta + 16u * c, o8);
+                dequant_word4<BF>(v[c].z, s2, b2, nibm, magic, &o8[0]);
+                dequant_word4<BF>(v[c].w, s2, b2, nibm, magic, &o8[4]);
+                tmem_st8(ta + 16u * c + 8u, o8);
             }
             tmem_st_wait();
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[sa]);
-            if (++sw == WS) {
-                sw = 0;
+            g += gstep2;
+            sw += 2;
+            w_off += 2u * w_stage_bytes;
+            sb_off += 2u * sb_stage_bytes;
+            if (sw >= WS) {
+                sw -= WS;
                 pw ^= 1;
+                w_off -= (uint32_t)WS * w_stage_bytes;
+                sb_off -= (uint32_t)WS * sb_stage_bytes;
             }
-            if (++sa == AS) {
-                sa = 0;
+            sa += 4;
+            if (sa >= AS) {
+                sa -= AS;
                 pa ^= 1;
             }
         }
@@ -664,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool split = p.plan.slots() > 1;
             float* pslot = p.partials + (int64_t)piece * p.M * p.N;
             const int nacc = nxs < NI ? nxs : NI;   // accumulators that received MMAs
-            for (int c = 8 * part; c < mt; c += 32) {
+            for (int c = 8 * grp; c < mt; c += 32) {
                 uint32_t v[8];
                 __syncwarp();
                 tmem_ld8(tmem_base + lane_base + acc_col + (uint32_t)c, v);
@@ -726,6 +757,7 @@ int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int gs) {
     (void)N;
     if (bits != 4) return 0;
     if (K % 64 != 0 || gs < 32) return 0;   // 64-column halves, whole groups
+    if (K > (int64_t)1 << 30) return 0;       // column offsets are kept in 32-bit registers
     return 1;
 }
 
@@ -786,10 +818,19 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     // (warp index % 4), which the dequantize and epilogue roles rely on; the
     // kernel also takes all 512 tensor-memory columns. The shared-memory
     // request is kept above half of the SM's capacity.
-    // two issuers (two accumulators) while they leave room for two A stages
-    const int ni = (tc::kMaxIssuers * mt + 2 * 128 <= kTmemCols) ? tc::kMaxIssuers : 1;
-    int as = (kTmemCols - ni * mt) / 128;
+    // Two issuers (two accumulators) while they leave room for four A stages
+    // (one per dequantize group). Ring depths and slot ownership: a ring slot
+    // must always be waited on by the same role, phase after phase, because
+    // mbarrier.try_wait.parity reports a phase two ahead of the barrier as
+    // complete. Hence, with two issuers taking alternate stages, the A and
+    // activation rings have even depth; the weight ring has even depth (two
+    // of the four dequantize groups read the even weight stages, two the odd
+    // ones); and the A ring holds at least the four stages of the four groups.
+    const int ni = (tc::kMaxIssuers * mt + 4 * (int)tc::kAStageCols <= kTmemCols) ? tc::kMaxIssuers : 1;
+    int as = (kTmemCols - ni * mt) / (int)tc::kAStageCols;
     as = as > kMaxAStages ? kMaxAStages : as;
+    if (ni == 2) as &= ~1;
+    if (as < 4) return cudaErrorInvalidValue;
     // one box of scales / biases per stage suffices when every piece starts on
     // a 256-column boundary (then so does every stage)
     int sb_boxes = 0;
@@ -809,14 +850,10 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     const size_t x_stage = (size_t)mt * tc::kXBK * 2;
     const size_t w_stage = (size_t)kTileN * kBK / 2 + 2u * tc::kSbBox * (size_t)sb_boxes;
     const size_t budget = 224 * 1024 - 1024 - kBars;
-    // With two issuers taking alternate activation stages the ring depth must
-    // be even: then every slot is always consumed by the same issuer, in order.
-    // (With an odd depth a slot passes between issuers, and an issuer more than
-    // a ring ahead of the other could wait on the parity of a phase that has
-    // not started, which mbarrier.try_wait.parity reports as complete.)
     const int xs_min = mt > 128 ? 2 : (ni == 2 ? 4 : 3);
     int ws = (int)((budget - (size_t)xs_min * x_stage) / w_stage);
-    ws = ws < 3 ? 3 : (ws > kMaxWStages ? kMaxWStages : ws);
+    ws = ws < 4 ? 4 : (ws > kMaxWStages ? kMaxWStages : ws);
+    ws &= ~1;
     int xs = (int)((budget - (size_t)ws * w_stage) / x_stage);
     xs = xs < 2 ? 2 : (xs > kMaxXStages ? kMaxXStages : xs);
     if (ni == 2) xs &= ~1;
@@ -842,7 +879,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.x_stages = xs;
     p.w_stages = ws;
     p.a_stages = as;
-    if (ni == 2 && (xs & 1)) return cudaErrorInvalidValue;   // slot ownership invariant above
+    if ((ni == 2 && ((xs | as) & 1)) || (ws & 1) || ws < 4) return cudaErrorInvalidValue;   // ring invariants above
     p.n_issuers = ni;
     p.sb_boxes = sb_boxes > 0 ? sb_boxes : 1;
     p.nib_mask = 0x000F000Fu;

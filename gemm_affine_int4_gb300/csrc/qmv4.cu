@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------- consumers: main loop ----------------
     const int g = warp / S, sl = warp % S;
-    const uint32_t mlo = a.mask_lo, mhi = a.mask_hi, one = a.one;
+    const uint32_t mlo = pin_reg(a.mask_lo), mhi = pin_reg(a.mask_hi), one = pin_reg(a.one);
     const int grp_off = (lane * 32) >> a.gs_log2;   // this lane's group within an iteration
     St* out = static_cast<St*>(a.out);
     int slot = 0, ph = 0;
