@@ -254,12 +254,22 @@ gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void*
 gai4_status gai4_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K, void* stream) {
     if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
     if (!aligned16(blocks) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    if (bq_tma_supported(BQ_Q8_0, N, K, blocks, x)) {
+        int* st = status_ptr();
+        if (!st) return GAI4_ERR_CUDA;
+        return from_cuda(launch_q8_0_gemv_tma(blocks, x, out, N, K, st, 2000000000LL, (cudaStream_t)stream));
+    }
     return from_cuda(launch_q8_0_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
 }
 
 gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K, void* stream) {
     if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 256 != 0) return GAI4_ERR_INVALID_ARG;
     if (!aligned16(blocks) || !aligned16(x)) return GAI4_ERR_MISALIGNED;
+    if (bq_tma_supported(BQ_Q4_K, N, K, blocks, x)) {
+        int* st = status_ptr();
+        if (!st) return GAI4_ERR_CUDA;
+        return from_cuda(launch_q4_k_gemv_tma(blocks, x, out, N, K, st, 2000000000LL, (cudaStream_t)stream));
+    }
     return from_cuda(launch_q4_k_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
 }
 

@@ -1,0 +1,523 @@
+// blockq_tma.cu -- Q8_0 and Q4_K matrix-vector products with TMA-staged
+// weight rows (sm_103a, CUDA cores; the work is HBM-bound).
+//
+// Formats (hanzo-kernel quant.rs, "Q8_0 PACKED matvec" and the Q4_K section):
+//  * Q8_0: a 36-byte block per 32 weights -- f16 scale d in the low half of
+//    word 0, then 32 signed int8 codes, four per word, byte 0 first;
+//    out[n] = sum_b d_b * sum_j q_j x_{32b+j}.
+//  * Q4_K: a 144-byte super-block per 256 weights -- d, dmin (f16), 12 bytes of
+//    eight 6-bit (sc, m) pairs (get_scale_min_k4), 128 bytes of codes; byte
+//    32g + i holds weight 64g + i (low nibble, sub-block 2g) and weight
+//    64g + 32 + i (high nibble, sub-block 2g + 1); a weight is d*sc*q - dmin*m.
+//
+// Design (one CTA per SM, persistent over row groups):
+//  * A row is cut into 1152-byte chunks: 32 Q8_0 blocks (1024 weights) or 8
+//    Q4_K super-blocks (2048 weights). A producer warp brings stages of
+//    rows x C chunks into a ring in shared memory with 2-D TMA boxes of
+//    rows x 1152 bytes (rows past N and bytes past the row end are filled
+//    with zeros, which decode to zero weights).
+//  * 16 consumer warps share every stage of 32 rows x 1 chunk (a warp two rows,
+//    a lane one item of the chunk: a Q8_0 block, or one 64-weight group g of a
+//    Q4_K super-block with its 16-byte header and 32 code bytes); a lane's
+//    activations are loaded once per chunk and serve both rows. (The code
+//    keeps the general form of S sets of G warps splitting K; the plan uses
+//    S = 1: a K split leaves sets idle when a row is a few chunks long.)
+//  * The activations are staged once per CTA in shared memory in an order in
+//    which the 32 lanes of a warp read consecutive 16-byte pieces, with the
+//    sum of every 32-element run.
+//  * Decoding places a code in the mantissa of a power of two with one shift
+//    and one three-input logic op. Q8_0: byte b of a word becomes 384 + q
+//    (exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80); sum q x
+//    = sum (384 + q) x - 384 sum x. Q4_K: one shift places the two nibbles of
+//    a byte at mantissa bits 15..18 and 19..22 of 1.0f, giving 1 + q_lo/256
+//    (sub-block 2g) and 1 + q_hi/16 (sub-block 2g + 1); a packed fp32 fma
+//    accumulates both against (x_i, x_{i+32}), starting from (-sum x_lo,
+//    -sum x_hi), so that sum q_lo x = 256 acc.x and sum q_hi x = 16 acc.y.
+//  * Per-row results of a set are held in a small shared buffer and combined
+//    over the sets in a fixed order every F row groups (one consumer barrier
+//    per flush, double-buffered): the result does not depend on timing.
+#include "common.cuh"
+#include "internal.h"
+#include "pipeline.cuh"
+
+namespace gai4 {
+
+namespace {
+
+using namespace pipe;
+
+constexpr int kCW = 16;                        // consumer warps
+constexpr int kThreads = 32 * (kCW + 1);       // + one producer warp
+constexpr uint32_t kChunkBytes = 1152;         // one row chunk
+constexpr int kChunkU64 = kChunkBytes / 8;     // TMA box width in 8-byte elements
+constexpr int kMaxDepth = 16;
+constexpr int kFlush = 8;                      // row groups per flush
+constexpr int kR = 2;                          // rows per consumer warp
+
+struct BqArgs {
+    int N;
+    int chunks;            // chunks per row (the last one may be partial)
+    int G, S, C;           // warps per set (kR rows each), consumer sets, chunks per stage
+    int cps, kss;          // chunks per set, stages per set and row group
+    int depth;
+    int n_groups;          // row groups = ceil(N / (kR G))
+    uint32_t stage_bytes;  // C * kR * G * 1152
+    uint32_t x_off, sum_off, pend_off, bar_off;   // shared-memory layout
+    const float* x;
+    float* out;
+    int K;
+    int* status;
+    long long spin_limit;
+};
+
+// (a & b) ^ c and (a & b) | c as one three-input logic instruction each
+__device__ __forceinline__ uint32_t lop3_andxor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// (acc.x + a_lo * b_lo, acc.y + a_hi * b_hi): two binary32 fmas in one instruction
+__device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo, float b_hi, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    const uint4 v = lds128(a);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
+
+// (sc, m) of sub-blocks j = 2g and 2g + 1 (get_scale_min_k4) from the 12
+// scale bytes held in three words b0 (bytes 0..3), b1 (4..7), b2 (8..11).
+// With t_i = b_i >> (8 (j & 3)), byte 0 of t_i belongs to sub-block 2g and
+// byte 1 to 2g + 1. For j < 4: sc = byte(b0) & 63, m = byte(b1) & 63; for
+// j >= 4: sc = (byte(b2) & 15) | (byte(b0) >> 6) << 4, m = (byte(b2) >> 4) |
+// (byte(b1) >> 6) << 4. Both forms are computed and one is selected (g is
+// fixed per lane, so there is no divergent branch).
+__device__ __forceinline__ void scale_min_pair(uint32_t b0, uint32_t b1, uint32_t b2, int g, float& sc0, float& m0,
+                                               float& sc1, float& m1) {
+    const int sh = 16 * (g & 1);
+    const uint32_t t0 = b0 >> sh, t1 = b1 >> sh, t2 = b2 >> sh;
+    const bool hi = g >= 2;
+    const uint32_t s0 = hi ? (t2 & 15u) | ((t0 >> 2) & 0x30u) : t0 & 63u;
+    const uint32_t s1 = hi ? ((t2 >> 8) & 15u) | ((t0 >> 10) & 0x30u) : (t0 >> 8) & 63u;
+    const uint32_t n0 = hi ? ((t2 >> 4) & 15u) | ((t1 >> 2) & 0x30u) : t1 & 63u;
+    const uint32_t n1 = hi ? ((t2 >> 12) & 15u) | ((t1 >> 10) & 0x30u) : (t1 >> 8) & 63u;
+    sc0 = (float)s0;
+    sc1 = (float)s1;
+    m0 = (float)n0;
+    m1 = (float)n1;
+}
+
+// ---------------------------------------------------------------------------
+// activation staging: x (f32, K) -> shared memory in lane order, zero past K
+// ---------------------------------------------------------------------------
+// Q8_0: chunk ch, block b (lane), piece j (4 elements): float4 index
+// (ch * 8 + j) * 32 + b; sums[32 ch + b] = sum of the block's 32 elements.
+// Q4_K: chunk ch, item u = 4 sb + g (lane), pair quad q (elements i = 2q,
+// 2q + 1 of both runs): float4 index (ch * 16 + q) * 32 + u holding
+// (x_lo[2q], x_hi[2q], x_lo[2q+1], x_hi[2q+1]); sums[8 (8 ch + sb) + j] = sum
+// of sub-block j (= sums[2 (32 ch + u)] and sums[2 (32 ch + u) + 1]).
+// One pass by the consumer threads: a thread takes 8 consecutive elements
+// of a 32-element run (Q8_0) or of both runs of a Q4_K item; the 4 threads of
+// a run sit in adjacent lanes and add their partial sums with shuffles.
+template <int FMT>
+__device__ void stage_x(const BqArgs& a, uint8_t* smem) {
+    float4* xs = reinterpret_cast<float4*>(smem + a.x_off);
+    float* sums = reinterpret_cast<float*>(smem + a.sum_off);
+    const int total = a.chunks * 128;   // a multiple of 32: whole warps in the shuffles
+    for (int v = threadIdx.x; v < total; v += kCW * 32) {
+        const int c = v >> 2, qq = v & 3;   // run (Q8_0 block) or item (Q4_K), quarter
+        const int ch = c >> 5, ln = c & 31;
+        if constexpr (FMT == BQ_Q8_0) {
+            const int k0 = 32 * c + 8 * qq;
+            float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+            if (k0 < a.K) {   // K is a multiple of 32: a run is all in or all out
+                f0 = *reinterpret_cast<const float4*>(a.x + k0);
+                f1 = *reinterpret_cast<const float4*>(a.x + k0 + 4);
+            }
+            xs[(ch * 8 + 2 * qq) * 32 + ln] = f0;
+            xs[(ch * 8 + 2 * qq + 1) * 32 + ln] = f1;
+            float t = ((f0.x + f0.y) + (f0.z + f0.w)) + ((f1.x + f1.y) + (f1.z + f1.w));
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            if (qq == 0) sums[c] = t;
+        } else {
+            // item ln = 4 sb + g of chunk ch: runs at base (low) and base + 32 (high)
+            const int base = ch * 2048 + 64 * ln, i0 = 8 * qq;
+            float lo[8], hi[8];
+            if (base < a.K) {   // K is a multiple of 256: an item is all in or all out
+                const float4 l0 = *reinterpret_cast<const float4*>(a.x + base + i0);
+                const float4 l1 = *reinterpret_cast<const float4*>(a.x + base + i0 + 4);
+                const float4 h0 = *reinterpret_cast<const float4*>(a.x + base + 32 + i0);
+                const float4 h1 = *reinterpret_cast<const float4*>(a.x + base + 32 + i0 + 4);
+                lo[0] = l0.x; lo[1] = l0.y; lo[2] = l0.z; lo[3] = l0.w;
+                lo[4] = l1.x; lo[5] = l1.y; lo[6] = l1.z; lo[7] = l1.w;
+                hi[0] = h0.x; hi[1] = h0.y; hi[2] = h0.z; hi[3] = h0.w;
+                hi[4] = h1.x; hi[5] = h1.y; hi[6] = h1.z; hi[7] = h1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) lo[j] = hi[j] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)   // pair quad 4 qq + q: elements i0 + 2q, i0 + 2q + 1
+                xs[(ch * 16 + 4 * qq + q) * 32 + ln] = make_float4(lo[2 * q], hi[2 * q], lo[2 * q + 1], hi[2 * q + 1]);
+            float sl = ((lo[0] + lo[1]) + (lo[2] + lo[3])) + ((lo[4] + lo[5]) + (lo[6] + lo[7]));
+            float sh = ((hi[0] + hi[1]) + (hi[2] + hi[3])) + ((hi[4] + hi[5]) + (hi[6] + hi[7]));
+            sl += __shfl_xor_sync(0xffffffffu, sl, 1);
+            sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+            sl += __shfl_xor_sync(0xffffffffu, sl, 2);
+            sh += __shfl_xor_sync(0xffffffffu, sh, 2);
+            if (qq == 0) {
+                sums[2 * c] = sl;       // sub-block 2g of super-block 8 ch + sb
+                sums[2 * c + 1] = sh;   // sub-block 2g + 1
+            }
+        }
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) bq_tma_kernel(const __grid_constant__ CUtensorMap wmap, const BqArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
+    uint64_t* empty = full + kMaxDepth;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxDepth);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = a.depth, S = a.S, G = a.G, C = a.C;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < D; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], G);   // the G warps of the set that owns the slot
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kCW && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
+    __syncthreads();   // barriers initialised: the producer starts while the consumers stage x
+    Ctl ctl{a.status, a.spin_limit, abort_flag};
+
+    // valid chunks of stage (set s, stage ks of the set): [c0, c0 + n)
+    auto stage_chunks = [&](int s, int ks, int& c0) {
+        c0 = s * a.cps + ks * C;
+        const int lim = min((s + 1) * a.cps, a.chunks);
+        return max(0, min(C, lim - c0));
+    };
+
+    if (warp == kCW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int slot = 0, ph = 0, issued = 0;
+            bool ok = true;
+            for (int rg = blockIdx.x; rg < a.n_groups && ok; rg += gridDim.x) {
+                for (int ks = 0; ks < a.kss && ok; ++ks) {
+                    for (int s = 0; s < S; ++s) {
+                        if (!mbar_wait(&empty[slot], (uint32_t)(ph ^ 1), ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        int c0;
+                        const int n = stage_chunks(s, ks, c0);
+                        mbar_arrive_expect_tx(&full[slot], (uint32_t)n * (uint32_t)(kR * G) * kChunkBytes);
+                        uint8_t* dst = smem + (size_t)slot * a.stage_bytes;
+                        for (int c = 0; c < n; ++c)
+                            tma_load_2d(dst + (size_t)c * (kR * G) * kChunkBytes, &wmap, &full[slot],
+                                        (c0 + c) * kChunkU64, rg * (kR * G));
+                        ++issued;
+                        if (++slot == D) {
+                            slot = 0;
+                            ph ^= 1;
+                        }
+                    }
+                }
+            }
+            // every issued copy has landed before the CTA may exit
+            for (int i = (issued > D ? issued - D : 0); i < issued; ++i)
+                mbar_wait_drain(&full[i % D], (uint32_t)((i / D) & 1), a.spin_limit, a.status);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    stage_x<FMT>(a, smem);
+    consumer_bar();
+    // warp wg of set s: rows kR * wg .. kR * wg + kR - 1 of every stage of the
+    // set; a lane's activations are loaded once per chunk and serve kR rows
+    const int s = warp / G, wg = warp % G;
+    const int RS = G * kR;
+    const uint32_t xs_base = smem_u32(smem + a.x_off);
+    const float* sums = reinterpret_cast<const float*>(smem + a.sum_off);
+    float* pend = reinterpret_cast<float*>(smem + a.pend_off);   // [2][kFlush][S][RS]
+    const uint32_t ring = smem_u32(smem);
+    // loop-invariant logic-op operands, held in registers
+    const uint32_t c_mask = pin_reg(FMT == BQ_Q8_0 ? 0x007F8000u : 0x00078000u);
+    const uint32_t c_mask2 = pin_reg(0x00780000u);
+    const uint32_t c_const = pin_reg(FMT == BQ_Q8_0 ? 0x43C00000u : 0x3F800000u);
+    int slot = s, ph = 0;   // this set's slots: s, s + S, ... (the depth is a multiple of S)
+    int buf = 0, fi = 0;
+    bool ok = true;
+    for (int rg = blockIdx.x; rg < a.n_groups; rg += gridDim.x) {
+        float part[kR];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) part[r] = 0.f;
+        for (int ks = 0; ks < a.kss; ++ks) {
+            if (ok && !warp_wait(&full[slot], (uint32_t)ph, ctl)) ok = false;
+            int c0;
+            const int n = ok ? stage_chunks(s, ks, c0) : 0;
+            const uint32_t st = ring + (uint32_t)slot * a.stage_bytes + (uint32_t)(wg * kR) * kChunkBytes;
+            for (int c = 0; c < n; ++c) {
+                const uint32_t rows = st + (uint32_t)c * (uint32_t)RS * kChunkBytes;   // row kR * wg of chunk c
+                const int ch = c0 + c;
+                if constexpr (FMT == BQ_Q8_0) {
+                    // block `lane` of the chunk: 9 words at 36 * lane (odd word
+                    // stride: no bank conflicts)
+                    const uint32_t xp = xs_base + (uint32_t)(ch * 8 * 32 + lane) * 16u;
+                    float4 xv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xv[i] = lds128f(xp + (uint32_t)i * 32u * 16u);
+                    const float xsum = sums[ch * 32 + lane];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+                        const uint32_t bp = rows + (uint32_t)r * kChunkBytes + 36u * (uint32_t)lane;
+                        const uint32_t hdr = lds32(bp);
+                        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t w = lds32(bp + 4u + 4u * (uint32_t)i);
+                            const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
+                            acc = ffma2(lop3_andxor(u0, c_mask, c_const), lop3_andxor(u1, c_mask, c_const), xv[i].x,
+                                        xv[i].y, acc);
+                            acc = ffma2(lop3_andxor(u2, c_mask, c_const), lop3_andxor(u3, c_mask, c_const), xv[i].z,
+                                        xv[i].w, acc);
+                        }
+                        part[r] = fmaf(f16_bits_to_f32(hdr), fmaf(-384.0f, xsum, acc.x + acc.y), part[r]);
+                    }
+                } else {
+                    // item lane = 4 sb + g: header of super-block sb, code bytes 32 g .. 32 g + 31
+                    const int sb = lane >> 2, g = lane & 3;
+                    const int sub = 8 * (ch * 8 + sb) + 2 * g;   // global sub-block of the low nibbles
+                    const float sx_lo = sums[sub], sx_hi = sums[sub + 1];
+                    float2 acc[kR];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) acc[r] = make_float2(-sx_lo, -sx_hi);
+                    const uint32_t xp = xs_base + (uint32_t)(ch * 16 * 32 + lane) * 16u;
+                    const uint32_t qoff = 144u * (uint32_t)sb + 16u + 32u * (uint32_t)g;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // code words 4h .. 4h + 3 (bytes i = 16h .. 16h + 15 of the run),
+                        // activation pairs (x_lo_i, x_hi_i) in pair quads 8h .. 8h + 7
+                        float4 xv[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) xv[q] = lds128f(xp + (uint32_t)(8 * h + q) * 32u * 16u);
+#pragma unroll
+                        for (int r = 0; r < kR; ++r) {
+                            const uint4 qv = lds128(rows + (uint32_t)r * kChunkBytes + qoff + 16u * (uint32_t)h);
+                            const uint32_t wv[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const uint32_t w = wv[t];
+                                const float4 p0 = xv[2 * t], p1 = xv[2 * t + 1];
+                                const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
+                                acc[r] = ffma2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const), p0.x,
+                                               p0.y, acc[r]);
+                                acc[r] = ffma2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const), p0.z,
+                                               p0.w, acc[r]);
+                                acc[r] = ffma2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const), p1.x,
+                                               p1.y, acc[r]);
+                                acc[r] = ffma2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const), p1.z,
+                                               p1.w, acc[r]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+                        const uint4 hdr = lds128(rows + (uint32_t)r * kChunkBytes + 144u * (uint32_t)sb);
+                        const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+                        float sc_lo, m_lo, sc_hi, m_hi;
+                        scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
+                        float v = part[r];
+                        v = fmaf(d * sc_lo, 256.0f * acc[r].x, v);
+                        v = fmaf(-(dmin * m_lo), sx_lo, v);
+                        v = fmaf(d * sc_hi, 16.0f * acc[r].y, v);
+                        v = fmaf(-(dmin * m_hi), sx_hi, v);
+                        part[r] = v;
+                    }
+                }
+            }
+            // the slot is refilled by TMA (async proxy): order these reads first, then release it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            slot += S;
+            if (slot >= D) {
+                slot -= D;
+                ph ^= 1;
+            }
+        }
+        // this set's sums for the warp's rows of the group, held until the next flush
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+            const float v = warp_sum(part[r]);
+            if (lane == 0) pend[((buf * kFlush + fi) * S + s) * RS + wg * kR + r] = v;
+        }
+        const bool last = rg + (int)gridDim.x >= a.n_groups;
+        if (++fi == kFlush || last) {
+            consumer_bar();
+            // rows of the flushed groups: sets added in order s = 0, 1, ...
+            const int nrows = fi * RS;
+            for (int t = threadIdx.x; t < nrows; t += kCW * 32) {
+                const int f = t / RS, r = t - f * RS;
+                float v = 0.f;
+                for (int ss = 0; ss < S; ++ss) v += pend[((buf * kFlush + f) * S + ss) * RS + r];
+                const int grp = rg - (fi - 1 - f) * (int)gridDim.x;
+                const int64_t n = (int64_t)grp * RS + r;
+                if (n < a.N) a.out[n] = v;
+            }
+            buf ^= 1;
+            fi = 0;
+        }
+    }
+}
+
+int num_sms_cached() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return sms;
+}
+
+// chooses G (rows per stage) by rounds x chunks per set, then C and the depth
+bool plan_bq(int64_t N, int chunks, int K, int fmt, BqArgs& a, size_t& smem) {
+    const int sms = num_sms_cached();
+    // One set of all consumer warps: every stage is a whole chunk of kR * 16
+    // rows (a K split between sets leaves sets idle when a row is a few
+    // chunks long, and halves the bytes in flight per set).
+    (void)sms;
+    const int bestG = kCW;
+    a.G = bestG;
+    a.S = kCW / bestG;
+    a.cps = (chunks + a.S - 1) / a.S;
+    a.C = std::min(a.cps, std::max(1, 8 / bestG));
+    a.kss = (a.cps + a.C - 1) / a.C;
+    a.chunks = chunks;
+    a.N = (int)N;
+    a.K = K;
+    a.n_groups = (int)((N + kR * a.G - 1) / (kR * a.G));
+    a.stage_bytes = (uint32_t)a.C * (uint32_t)(kR * a.G) * kChunkBytes;
+    const size_t x_bytes = (size_t)chunks * (fmt == BQ_Q8_0 ? 1024 : 2048) * 4;
+    const size_t sum_bytes = (size_t)chunks * 32 * (fmt == BQ_Q8_0 ? 1 : 2) * 4;
+    const size_t pend_bytes = (size_t)2 * kFlush * kCW * kR * 4;
+    const size_t bar_bytes = 2 * kMaxDepth * 8 + 16;
+    const size_t fixed = 128 + x_bytes + sum_bytes + pend_bytes + bar_bytes;
+    const size_t cap = 227 * 1024;
+    if (fixed + 2 * (size_t)a.S * a.stage_bytes > cap) return false;
+    int D = (int)((cap - fixed) / a.stage_bytes);
+    D = std::min(D, kMaxDepth);
+    D -= D % a.S;   // slot s is always read by set s % S
+    if (D < 2 * a.S) return false;
+    a.depth = D;
+    size_t off = (size_t)D * a.stage_bytes;   // ring first (128-byte aligned base)
+    a.x_off = (uint32_t)off;
+    off += x_bytes;
+    a.sum_off = (uint32_t)off;
+    off += sum_bytes;
+    a.pend_off = (uint32_t)off;
+    off += pend_bytes;
+    off = (off + 7) & ~(size_t)7;
+    a.bar_off = (uint32_t)off;
+    off += bar_bytes;
+    smem = off + 128;
+    return smem <= cap;
+}
+
+template <int FMT>
+cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N, int64_t K, size_t row_bytes,
+                      int* status, long long spin_limit, cudaStream_t stream) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int chunks = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
+    BqArgs a;
+    size_t smem = 0;
+    if (!plan_bq(N, chunks, (int)K, FMT, a, smem)) return cudaErrorNotSupported;
+    CUtensorMap wmap;
+    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)kChunkU64, (cuuint32_t)(kR * a.G)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(blocks), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    a.x = x;
+    a.out = out;
+    a.status = status;
+    a.spin_limit = spin_limit;
+    if (!a.status) return cudaErrorInvalidValue;
+    static unsigned long long configured = 0ull;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(configured & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(bq_tma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured |= 1ull << dev;
+    }
+    const int grid = (int)std::min<int64_t>(a.n_groups, num_sms_cached());
+    bq_tma_kernel<FMT><<<grid, kThreads, smem, stream>>>(wmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Rows must start on 16-byte boundaries (TMA) and the staged activations must
+// fit in shared memory next to a ring of at least two stages per set.
+bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const float* x) {
+    if (N <= 0 || N > (int64_t)1 << 30 || K <= 0 || K > (int64_t)1 << 20) return false;
+    if (((uintptr_t)blocks & 15u) || ((uintptr_t)x & 15u)) return false;
+    const size_t row_bytes = fmt == BQ_Q8_0 ? (size_t)K / 32 * 36 : (size_t)K / 256 * 144;
+    if (row_bytes % 16 != 0) return false;
+    if (!encode_fn()) return false;
+    BqArgs a;
+    size_t smem = 0;
+    const int chunks = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
+    return plan_bq(N, chunks, (int)K, fmt, a, smem);
+}
+
+cudaError_t launch_q8_0_gemv_tma(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K,
+                                 int* status, long long spin_limit, cudaStream_t s) {
+    return launch_bq<BQ_Q8_0>(blocks, x, out, N, K, (size_t)K / 32 * 36, status, spin_limit, s);
+}
+cudaError_t launch_q4_k_gemv_tma(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
+                                 int* status, long long spin_limit, cudaStream_t s) {
+    return launch_bq<BQ_Q4_K>(blocks, x, out, N, K, (size_t)K / 256 * 144, status, spin_limit, s);
+}
+
+}  // namespace gai4

@@ -84,7 +84,16 @@ cudaError_t launch_dequantize(const uint32_t* packed, const void* scales, const 
 cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N,
                                  const SplitPlan& plan, int dtype, cudaStream_t s);
 
-// block-quantized GEMVs (blockq.cu)
+// block-quantized GEMVs with TMA-staged rows (blockq_tma.cu): supported when
+// rows start on 16-byte boundaries and the activations fit in shared memory
+enum { BQ_Q8_0 = 0, BQ_Q4_K = 1 };
+bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const float* x);
+cudaError_t launch_q8_0_gemv_tma(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K,
+                                 int* status, long long spin_limit, cudaStream_t s);
+cudaError_t launch_q4_k_gemv_tma(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
+                                 int* status, long long spin_limit, cudaStream_t s);
+
+// block-quantized GEMVs, general case (blockq.cu)
 cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N,
                              int64_t K, cudaStream_t s);
 cudaError_t launch_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N,

@@ -56,6 +56,40 @@ def test_q4_k_small(N, K):
     assert_within(got, ref, absdot, "f32", f"q4_k N={N} K={K}")
 
 
+# Row lengths that are multiples of 16 bytes take the TMA-staged kernel (one or
+# several 1152-byte chunks per row, a partial last chunk, row counts that are
+# not multiples of the rows per stage); K = 65536 does not fit the staged
+# activations and takes the general kernel, as do Q8_0 rows of 36 * odd bytes.
+@pytest.mark.parametrize("N,K", [(1, 128), (17, 2048), (1000, 2048), (77, 5632), (1029, 3072), (3, 65536)])
+def test_q8_0_staged_shapes(N, K):
+    blocks = synth.q8_0_blocks(N, K, seed=N * 7 + K)
+    x = synth.f32_vector(K, seed=K + 5)
+    ref, absdot = oracle.q8_0_gemv(blocks, x)
+    got = g4.gai4_q8_0_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert_within(got, ref, absdot, "f32", f"q8_0 N={N} K={K}")
+
+
+@pytest.mark.parametrize("N,K", [(1, 2048), (17, 2304), (1000, 4096), (77, 5376), (4099, 3072), (3, 65536)])
+def test_q4_k_staged_shapes(N, K):
+    blocks = synth.q4_k_blocks(N, K, seed=N * 5 + K)
+    x = synth.f32_vector(K, seed=K + 9)
+    ref, absdot = oracle.q4_k_gemv(blocks, x)
+    got = g4.gai4_q4_k_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert_within(got, ref, absdot, "f32", f"q4_k N={N} K={K}")
+
+
+def test_blockq_repeatable():
+    """The per-row sums are combined in a fixed order: repeated calls agree bit for bit."""
+    N, K = 3000, 5120
+    for kind in ("q8_0", "q4_k"):
+        blocks = synth.q8_0_blocks(N, K, 41) if kind == "q8_0" else synth.q4_k_blocks(N, K, 41)
+        fn = g4.gai4_q8_0_gemv if kind == "q8_0" else g4.gai4_q4_k_gemv
+        b, x = to_dev(blocks), to_dev(synth.f32_vector(K, 42))
+        first = fn(b, x).cpu().numpy()
+        for _ in range(5):
+            assert np.array_equal(fn(b, x).cpu().numpy(), first), kind
+
+
 def test_q4_k_element_order_one_hot():
     """x = e_k picks weight k of every row: checks the nibble / sub-block order."""
     N, K = 4, 256
