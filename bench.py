@@ -53,8 +53,8 @@ _CSRC = "gemm_affine_int4_gb300/csrc/"
 KERNEL_SOURCES = {
     "qmv": [_CSRC + f for f in ("qmv4.cu", "pipeline.cuh", "common.cuh", "api.cu")],
     "qmm_t": [_CSRC + f for f in ("qmm_tc.cu", "pipeline.cuh", "common.cuh", "api.cu")],
-    "q8_0": [_CSRC + f for f in ("blockq.cu", "common.cuh", "api.cu")],
-    "q4_k": [_CSRC + f for f in ("blockq.cu", "common.cuh", "api.cu")],
+    "q8_0": [_CSRC + f for f in ("blockq_tma.cu", "blockq.cu", "pipeline.cuh", "common.cuh", "api.cu")],
+    "q4_k": [_CSRC + f for f in ("blockq_tma.cu", "blockq.cu", "pipeline.cuh", "common.cuh", "api.cu")],
 }
 
 
@@ -375,8 +375,9 @@ def run_gpu(args, rank, world, local_rank):
         "breakdown": {fam: {"ms": round(fam_ms[fam], 5), "GB/s": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9, 1),
                             "frac_of_hbm": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9 / hbm, 3),
                             "bytes": fam_bytes[fam]} for fam in fams},
-        "roofline": {"kernel": {"qmv": "affine_gemv_kernel (qmv, M=1)", "qmm_t": "qmm_t family",
-                                "q8_0": "q8_0_gemv_kernel", "q4_k": "q4_k_gemv_kernel"}[dom],
+        "roofline": {"kernel": {"qmv": "qmv4_kernel (qmv, M=1)",
+                                "qmm_t": "qmm_t family (qmm_tc4_kernel + splitk_reduce)",
+                                "q8_0": "q8_0_tma_kernel", "q4_k": "q4_k_tma_kernel"}[dom],
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "launches_per_step": n_launch,

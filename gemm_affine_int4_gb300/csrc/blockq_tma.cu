@@ -200,7 +200,7 @@ __device__ void stage_x(const BqArgs& a, uint8_t* smem) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) bq_tma_kernel(const __grid_constant__ CUtensorMap wmap, const BqArgs a) {
+__device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArgs& a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
@@ -403,6 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1) bq_tma_kernel(const __grid_consta
     }
 }
 
+__global__ void __launch_bounds__(kThreads, 1) q8_0_tma_kernel(const __grid_constant__ CUtensorMap wmap, const BqArgs a) {
+    bq_tma_body<BQ_Q8_0>(wmap, a);
+}
+__global__ void __launch_bounds__(kThreads, 1) q4_k_tma_kernel(const __grid_constant__ CUtensorMap wmap, const BqArgs a) {
+    bq_tma_body<BQ_Q4_K>(wmap, a);
+}
+
 int num_sms_cached() {
     static int sms = 0;
     if (!sms) {
@@ -481,17 +488,19 @@ cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N,
     a.status = status;
     a.spin_limit = spin_limit;
     if (!a.status) return cudaErrorInvalidValue;
-    static unsigned long long configured = 0ull;
+    using KernFn = void (*)(const CUtensorMap, const BqArgs);
+    const KernFn kern = FMT == BQ_Q8_0 ? q8_0_tma_kernel : q4_k_tma_kernel;
+    static unsigned long long configured = 0ull;   // bit (2 * device + format)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 64 || !(configured & (1ull << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(bq_tma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+    const int bit = 2 * dev + FMT;
+    if (bit >= 64 || !(configured & (1ull << bit))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
-        if (dev < 64) configured |= 1ull << dev;
+        if (bit < 64) configured |= 1ull << bit;
     }
     const int grid = (int)std::min<int64_t>(a.n_groups, num_sms_cached());
-    bq_tma_kernel<FMT><<<grid, kThreads, smem, stream>>>(wmap, a);
+    kern<<<grid, kThreads, smem, stream>>>(wmap, a);
     return cudaGetLastError();
 }
 
