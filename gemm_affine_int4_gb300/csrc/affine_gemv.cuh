@@ -241,6 +241,8 @@ struct AffineKernelArgs {
 
 template <typename T, int BITS, int R, int MB, int NW>
 __global__ void __launch_bounds__(NW * 32) affine_gemv_kernel(const AffineKernelArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     using Path = typename PathFor<T, BITS>::type;
     using St = typename T::storage;
     constexpr int E = Path::E, CW = Path::CW, NP = Path::NP;
@@ -434,8 +436,7 @@ cudaError_t launch_affine_gemv_t(const AffineGemvLaunch& L, cudaStream_t stream)
     a.KSP = KSP;
     const int rows_per_cta = (NW / L.ksplit) * R;
     dim3 grid((unsigned)((L.N + rows_per_cta - 1) / rows_per_cta), (unsigned)((L.M + MB - 1) / MB));
-    affine_gemv_kernel<T, BITS, R, MB, NW><<<grid, NW * 32, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(affine_gemv_kernel<T, BITS, R, MB, NW>, grid, dim3(NW * 32), smem, stream, a);
 }
 
 // dispatch over (rows per warp, x rows per CTA) for one (T, BITS)

@@ -44,6 +44,8 @@ template <int R>
 __global__ void __launch_bounds__(kNW * 32) q8_0_gemv_kernel(const uint32_t* __restrict__ blocks,
                                                              const float* __restrict__ x, float* __restrict__ out,
                                                              int64_t N, int64_t K, int S, int KS) {
+    pdl_launch_dependents();
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     constexpr int PPC = 8;   // 16-byte pieces of activations per 32-element chunk
     const int KSP = (KS + 1023) / 1024 * 1024;   // whole warp iterations (32 chunks)
     extern __shared__ uint4 smem[];
@@ -202,6 +204,8 @@ template <int R>
 __global__ void __launch_bounds__(kNW * 32) q4_k_gemv_kernel(const uint8_t* __restrict__ blocks,
                                                              const float* __restrict__ x, float* __restrict__ out,
                                                              int64_t N, int64_t K, int S, int KS) {
+    pdl_launch_dependents();
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     constexpr int PPC = 8;
     const int KSP = (KS + 1023) / 1024 * 1024;   // whole warp iterations (32 chunks)
     extern __shared__ uint4 smem[];
@@ -372,8 +376,7 @@ cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out,
     cudaError_t e = set_smem(q8_0_gemv_kernel<kRows>);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((N + rows_per_cta - 1) / rows_per_cta);
-    q8_0_gemv_kernel<kRows><<<grid, kNW * 32, smem, s>>>(blocks, x, out, N, K, S, KS);
-    return cudaGetLastError();
+    return launch_pdl(q8_0_gemv_kernel<kRows>, dim3(grid), dim3(kNW * 32), smem, s, blocks, x, out, N, K, S, KS);
 }
 
 cudaError_t launch_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
@@ -390,8 +393,7 @@ cudaError_t launch_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, 
     cudaError_t e = set_smem(q4_k_gemv_kernel<kRows>);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((N + rows_per_cta - 1) / rows_per_cta);
-    q4_k_gemv_kernel<kRows><<<grid, kNW * 32, smem, s>>>(blocks, x, out, N, K, S, KS);
-    return cudaGetLastError();
+    return launch_pdl(q4_k_gemv_kernel<kRows>, dim3(grid), dim3(kNW * 32), smem, s, blocks, x, out, N, K, S, KS);
 }
 
 }  // namespace gai4

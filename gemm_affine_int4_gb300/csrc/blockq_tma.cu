@@ -202,6 +202,7 @@ __device__ void stage_x(const BqArgs& a, uint8_t* smem) {
 template <int FMT>
 __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArgs& a) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
     uint64_t* empty = full + kMaxDepth;
@@ -219,6 +220,7 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
     }
     if (warp == kCW && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
     __syncthreads();   // barriers initialised: the producer starts while the consumers stage x
+    pdl_wait();        // the kernels before this one are complete: global memory may be read
     Ctl ctl{a.status, a.spin_limit, abort_flag};
 
     // valid chunks of stage (set s, stage ks of the set): [c0, c0 + n)
@@ -500,8 +502,7 @@ cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N,
         if (bit < 64) configured |= 1ull << bit;
     }
     const int grid = (int)std::min<int64_t>(a.n_groups, num_sms_cached());
-    kern<<<grid, kThreads, smem, stream>>>(wmap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, wmap, a);
 }
 
 }  // namespace

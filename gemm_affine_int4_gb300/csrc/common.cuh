@@ -6,9 +6,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/gai4.h"
 
 namespace gai4 {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. The hot-path kernels are launched so that
+// the next kernel in the stream may start (its launch and set-up: barriers,
+// tensor-memory allocation) while this one finishes: every kernel lets its
+// dependents be scheduled at entry, and waits for the kernels before it to
+// complete -- with their memory visible -- before its first global-memory
+// access. A kernel that reads another call's output is therefore ordered
+// exactly as with plain stream order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // dtype traits: storage type, conversion to/from binary32

@@ -61,6 +61,8 @@ namespace gai4 {
 template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ P, typename T::storage* __restrict__ out, int64_t M,
                                      int64_t N, SplitPlan plan) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t MN = M * N;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= MN) return;
@@ -77,6 +79,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ P, typename T::st
 template <typename T>
 __global__ void splitk_reduce8_kernel(const float* __restrict__ P, typename T::storage* __restrict__ out, int64_t M,
                                       int64_t N, SplitPlan plan) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t MN = M * N;
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // chunk of 8 outputs
     if (c >= MN / 8) return;
@@ -106,29 +110,27 @@ __global__ void splitk_reduce8_kernel(const float* __restrict__ P, typename T::s
 }
 
 template <typename T>
-static void reduce_launch(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
-                          cudaStream_t s) {
+static cudaError_t reduce_launch(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
+                                 cudaStream_t s) {
     auto* o = static_cast<typename T::storage*>(out);
     const int64_t MN = M * N;
     const bool vec = N % 8 == 0 && (reinterpret_cast<uintptr_t>(partials) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     if (vec) {
         const unsigned blocks = (unsigned)((MN / 8 + 255) / 256);
-        splitk_reduce8_kernel<T><<<blocks, 256, 0, s>>>(partials, o, M, N, plan);
-    } else {
-        const unsigned blocks = (unsigned)((MN + 255) / 256);
-        splitk_reduce_kernel<T><<<blocks, 256, 0, s>>>(partials, o, M, N, plan);
+        return launch_pdl(splitk_reduce8_kernel<T>, dim3(blocks), dim3(256), 0, s, partials, o, M, N, plan);
     }
+    const unsigned blocks = (unsigned)((MN + 255) / 256);
+    return launch_pdl(splitk_reduce_kernel<T>, dim3(blocks), dim3(256), 0, s, partials, o, M, N, plan);
 }
 
 cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N, const SplitPlan& plan,
                                  int dtype, cudaStream_t s) {
     switch (dtype) {
-    case GAI4_F16: reduce_launch<F16>(partials, out, M, N, plan, s); break;
-    case GAI4_F32: reduce_launch<F32>(partials, out, M, N, plan, s); break;
-    default: reduce_launch<BF16>(partials, out, M, N, plan, s); break;
+    case GAI4_F16: return reduce_launch<F16>(partials, out, M, N, plan, s);
+    case GAI4_F32: return reduce_launch<F32>(partials, out, M, N, plan, s);
+    default: return reduce_launch<BF16>(partials, out, M, N, plan, s);
     }
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -395,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap bmap,
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();
     // 1024-byte aligned base (128-byte swizzle atoms)
     // pointer arithmetic on the shared array keeps accesses in the shared state space
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -457,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     const uint32_t acc_col = 0;   // accumulator of issuer j: columns [j * mt, (j + 1) * mt)
     const int NI = p.n_issuers;
     const uint32_t a_col0 = (uint32_t)kTmemCols - kAStageCols * (uint32_t)AS;   // A ring at the top
@@ -902,8 +906,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
         if (dev < 64) configured[which] |= 1ull << dev;
     }
     dim3 grid((unsigned)L.plan.pieces(), 1u, (unsigned)mchunks);
-    kern<<<grid, kThreads, smem, stream>>>(wmap, xmap, smap, bmap, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), smem, stream, wmap, xmap, smap, bmap, p);
 }
 
 }  // namespace gai4

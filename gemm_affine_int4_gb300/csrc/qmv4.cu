@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap bmap, const Qmv4Args a) {
     using St = typename T::storage;
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();
     // 128-byte aligned base (TMA destinations); pointer arithmetic on the
     // shared array keeps the accesses below in the shared state space
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     Ctl ctl{a.status, a.spin_limit, abort_flag};
 
     if (warp == kCWarps) {
@@ -387,8 +389,7 @@ cudaError_t launch_t(const CUtensorMap& wm, const CUtensorMap& sm, const CUtenso
         if (dev < 64) configured |= 1ull << dev;
     }
     const int64_t grid = std::min<int64_t>(a.n_blocks, num_sms());
-    qmv4_kernel<T, R><<<(unsigned)grid, kThreads, smem, s>>>(wm, sm, bm, a);
-    return cudaGetLastError();
+    return launch_pdl(qmv4_kernel<T, R>, dim3((unsigned)grid), dim3(kThreads), smem, s, wm, sm, bm, a);
 }
 
 template <typename T>
