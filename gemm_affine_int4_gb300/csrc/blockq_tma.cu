@@ -218,17 +218,28 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kCW && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
-    __syncthreads();   // barriers initialised: the producer starts while the consumers stage x
-    pdl_wait();        // the kernels before this one are complete: global memory may be read
-    Ctl ctl{a.status, a.spin_limit, abort_flag};
-
     // valid chunks of stage (set s, stage ks of the set): [c0, c0 + n)
     auto stage_chunks = [&](int s, int ks, int& c0) {
         c0 = s * a.cps + ks * C;
         const int lim = min((s + 1) * a.cps, a.chunks);
         return max(0, min(C, lim - c0));
     };
+    // Warm L2 with the first ring-full of stages while the barriers are set up
+    // and the kernels before this one finish; the copies start after that wait.
+    if (warp == kCW && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
+        int cnt = 0;
+        for (int rg = blockIdx.x; rg < a.n_groups && cnt < D; rg += gridDim.x)
+            for (int ks = 0; ks < a.kss && cnt < D; ++ks)
+                for (int s = 0; s < S && cnt < D; ++s, ++cnt) {
+                    int c0;
+                    const int n = stage_chunks(s, ks, c0);
+                    for (int c = 0; c < n; ++c) tma_prefetch_2d(&wmap, (c0 + c) * kChunkU64, rg * (kR * G));
+                }
+    }
+    __syncthreads();   // barriers initialised: the producer starts while the consumers stage x
+    pdl_wait();        // the kernels before this one are complete: global memory may be read
+    Ctl ctl{a.status, a.spin_limit, abort_flag};
 
     if (warp == kCW) {
         // ---------------- producer ----------------

@@ -432,6 +432,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
     const int nas = nxs;                                       // = A stages
 
+    // Warm L2 with the first ring-full of weight stages (and their scales /
+    // biases) while the barriers and tensor memory are set up and the kernels
+    // before this one finish; the copies themselves start after that wait.
+    if (warp == 1 && lane == 0) {
+        for (int i = 0; i < nst && i < WS; ++i) {
+            const int64_t kst = k_begin + (int64_t)kBK * i;
+            tma_prefetch_2d(&wmap, (int)(kst / 8), (int)n0);
+            if constexpr (SBT) {
+                int x0 = 0, nbox = 0;
+                stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
+                for (int bx = 0; bx < nbox; ++bx) {
+                    tma_prefetch_2d(&smap, x0 + 8 * bx, (int)n0);
+                    tma_prefetch_2d(&bmap, x0 + 8 * bx, (int)n0);
+                }
+            }
+        }
+    }
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < WS; ++i) {
             mbar_init(&w_full[i], 1);

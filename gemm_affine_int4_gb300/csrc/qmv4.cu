@@ -122,6 +122,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t my_blocks =
         a.n_blocks > (int64_t)blockIdx.x ? (a.n_blocks - 1 - (int64_t)blockIdx.x) / gridDim.x + 1 : 0;
 
+    // Warm L2 with the first ring-full of stages while the barriers are set up
+    // and the kernels before this one finish; the copies start after that wait.
+    if (warp == kCWarps && lane == 0) {
+        int cnt = 0;
+        for (int64_t b = 0; b < my_blocks && cnt < D; ++b) {
+            const int row0 = (int)(((int64_t)blockIdx.x + b * gridDim.x) * BR);
+            for (int j = 0; j < n_st && cnt < D; ++j, ++cnt) {
+                const int it0 = j * S;
+                const int nsl = min(S, n_it - it0);
+                if (a.box3) {
+                    tma_prefetch_3d(&wmap, 0, it0, row0);
+                    tma_prefetch_3d(&smap, 0, it0, row0);
+                    tma_prefetch_3d(&bmap, 0, it0, row0);
+                } else {
+                    for (int ss = 0; ss < nsl; ++ss) {
+                        const int it = it0 + ss;
+                        tma_prefetch_2d(&wmap, it * (kItCols / 8), row0);
+                        tma_prefetch_2d(&smap, it * a.sbg, row0);
+                        tma_prefetch_2d(&bmap, it * a.sbg, row0);
+                    }
+                }
+            }
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < D; ++i) {
             mbar_init(&full[i], 1);
