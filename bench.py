@@ -257,6 +257,19 @@ def kernel_launches_per_step(g4, calls, torch):
     return n
 
 
+def max_over_ranks(torch, dist, x, device):
+    """The slowest rank's value (every rank gets it): the job's step time."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job GB/s: every replica moves the same step bytes (weak scaling),
+    and the job's step takes the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import gemm_affine_int4_gb300 as g4
@@ -346,10 +359,8 @@ def run_gpu(args, rank, world, local_rank):
 
     ms_per_step = elapsed_ms / steps_total
     if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * total_bytes / (ms_per_step * 1e-3) / 1e9
+        ms_per_step = max_over_ranks(torch, dist, ms_per_step, dev)
+    value = job_throughput(world, total_bytes, ms_per_step)
 
     hbm, tflops, peak_src = load_peaks()
     dom = max(fam_ms, key=fam_ms.get)
