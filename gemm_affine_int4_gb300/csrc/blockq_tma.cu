@@ -66,6 +66,7 @@ struct BqArgs {
     const float* x;
     float* out;
     int K;
+    int last_half;         // Q4_K: the last chunk holds at most 4 super-blocks
     int* status;
     long long spin_limit;
 };
@@ -329,6 +330,49 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                         }
                         part[r] = fmaf(f16_bits_to_f32(hdr), fmaf(-384.0f, xsum, acc.x + acc.y), part[r]);
                     }
+                } else if (ch == a.chunks - 1 && a.last_half) {
+                    // A last chunk of at most 4 super-blocks (16 items): lanes
+                    // 16..31 take the warp's second row instead of zero-filled items.
+                    const int it = lane & 15, rr = lane >> 4;
+                    const int sb = it >> 2, g = it & 3;
+                    const int sub = 8 * (ch * 8 + sb) + 2 * g;
+                    const float sx_lo = sums[sub], sx_hi = sums[sub + 1];
+                    float2 acc = make_float2(-sx_lo, -sx_hi);
+                    const uint32_t xp = xs_base + (uint32_t)(ch * 16 * 32 + it) * 16u;
+                    const uint32_t rowa = rows + (uint32_t)rr * kChunkBytes;
+                    const uint32_t qoff = 144u * (uint32_t)sb + 16u + 32u * (uint32_t)g;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 qv = lds128(rowa + qoff + 16u * (uint32_t)h);
+                        const uint32_t wv[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float4 p0 = lds128f(xp + (uint32_t)(8 * h + 2 * t) * 32u * 16u);
+                            const float4 p1 = lds128f(xp + (uint32_t)(8 * h + 2 * t + 1) * 32u * 16u);
+                            const uint32_t w = wv[t];
+                            const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
+                            acc = ffma2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const), p0.x, p0.y,
+                                        acc);
+                            acc = ffma2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const), p0.z, p0.w,
+                                        acc);
+                            acc = ffma2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const), p1.x, p1.y,
+                                        acc);
+                            acc = ffma2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const), p1.z, p1.w,
+                                        acc);
+                        }
+                    }
+                    const uint4 hdr = lds128(rowa + 144u * (uint32_t)sb);
+                    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+                    float sc_lo, m_lo, sc_hi, m_hi;
+                    scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
+                    float v = 0.f;
+                    v = fmaf(d * sc_lo, 256.0f * acc.x, v);
+                    v = fmaf(-(dmin * m_lo), sx_lo, v);
+                    v = fmaf(d * sc_hi, 16.0f * acc.y, v);
+                    v = fmaf(-(dmin * m_hi), sx_hi, v);
+                    static_assert(kR == 2, "the half-chunk mapping pairs the warp's two rows");
+                    part[0] += rr == 0 ? v : 0.f;
+                    part[1] += rr == 1 ? v : 0.f;
                 } else {
                     // item lane = 4 sb + g: header of super-block sb, code bytes 32 g .. 32 g + 31
                     const int sb = lane >> 2, g = lane & 3;
@@ -450,6 +494,8 @@ bool plan_bq(int64_t N, int chunks, int K, int fmt, BqArgs& a, size_t& smem) {
     a.chunks = chunks;
     a.N = (int)N;
     a.K = K;
+    const int sb_last = (K / 256) % 8;
+    a.last_half = fmt == BQ_Q4_K && sb_last != 0 && sb_last <= 4;
     a.n_groups = (int)((N + kR * a.G - 1) / (kR * a.G));
     a.stage_bytes = (uint32_t)a.C * (uint32_t)(kR * a.G) * kChunkBytes;
     const size_t x_bytes = (size_t)chunks * (fmt == BQ_Q8_0 ? 1024 : 2048) * 4;
