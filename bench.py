@@ -430,7 +430,7 @@ def call_name(c):
 def time_per_call(torch, g4, calls, stream, fams, reps=10):
     """Each call alone (its own CUDA graph), cold L2: a 256 MB buffer is
     overwritten before every timed replay. Reported beside the step timing."""
-    hbm, _, _ = load_peaks()
+    hbm, tflops, _ = load_peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=stream.device)
     out = []
     for fam in fams:
@@ -452,8 +452,16 @@ def time_per_call(torch, g4, calls, stream, fams, reps=10):
             us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts[2:])
             med = us[len(us) // 2]
             gbs = c["bytes"] / (med * 1e-6) / 1e9
-            out.append({"call": call_name(c), "us": round(med, 3), "GB/s": round(gbs, 1),
-                        "frac_of_hbm": round(gbs / hbm, 3)})
+            rec = {"call": call_name(c), "us": round(med, 3), "GB/s": round(gbs, 1),
+                   "frac_of_hbm": round(gbs / hbm, 3)}
+            if c["kind"] == "qmm_t":
+                # min(HBM, tensor) roofline: the call cannot beat the larger of
+                # its byte time and its bf16 tensor-core time
+                flops = 2.0 * c["M"] * c["N"] * c["K"]
+                roof_us = max(c["bytes"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+                rec.update({"TFLOP/s": round(flops / (med * 1e-6) / 1e12, 2),
+                            "frac_of_roofline": round(roof_us / med, 3)})
+            out.append(rec)
     del flush
     return out
 
