@@ -427,40 +427,52 @@ def call_name(c):
     return f"{c['kind']} N{c['N']}xK{c['K']}"
 
 
-def time_per_call(torch, g4, calls, stream, fams, reps=10):
-    """Each call alone (its own CUDA graph), cold L2: a 256 MB buffer is
-    overwritten before every timed replay. Reported beside the step timing."""
+def time_per_call(torch, g4, calls, stream, fams, reps=8):
+    """Each call alone with a cold L2: a graph of `reps` x [overwrite a 256 MB
+    buffer, the call] minus a graph of `reps` x [overwrite] (the same flushes),
+    divided by `reps`: the call's own time, without graph-launch latency.
+    Reported beside the step timing."""
     hbm, tflops, _ = load_peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=stream.device)
+
+    def graph_us(body):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for r in range(reps):
+                body(r)
+        best = None
+        with torch.cuda.stream(stream):
+            gr.replay()
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
+            stream.synchronize()
+            t = e0.elapsed_time(e1) * 1e3
+            best = t if best is None else min(best, t)
+        return best
+
+    flush_only = graph_us(lambda r: flush.fill_(float(r)))
     out = []
     for fam in fams:
         for c in calls[fam]:
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
+            def body(r, c=c):
+                flush.fill_(float(r))
                 issue(g4, c)
-            ts = []
-            with torch.cuda.stream(stream):
-                for r in range(reps + 2):
-                    flush.fill_(float(r))
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    gr.replay()
-                    e1.record(stream)
-                    ts.append((e0, e1))
-            stream.synchronize()
-            us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts[2:])
-            med = us[len(us) // 2]
-            gbs = c["bytes"] / (med * 1e-6) / 1e9
-            rec = {"call": call_name(c), "us": round(med, 3), "GB/s": round(gbs, 1),
+            us = max((graph_us(body) - flush_only) / reps, 1e-3)
+            gbs = c["bytes"] / (us * 1e-6) / 1e9
+            rec = {"call": call_name(c), "us": round(us, 3), "GB/s": round(gbs, 1),
                    "frac_of_hbm": round(gbs / hbm, 3)}
             if c["kind"] == "qmm_t":
                 # min(HBM, tensor) roofline: the call cannot beat the larger of
                 # its byte time and its bf16 tensor-core time
                 flops = 2.0 * c["M"] * c["N"] * c["K"]
                 roof_us = max(c["bytes"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-                rec.update({"TFLOP/s": round(flops / (med * 1e-6) / 1e12, 2),
-                            "frac_of_roofline": round(roof_us / med, 3)})
+                rec.update({"TFLOP/s": round(flops / (us * 1e-6) / 1e12, 2),
+                            "frac_of_roofline": round(roof_us / us, 3)})
             out.append(rec)
     del flush
     return out
