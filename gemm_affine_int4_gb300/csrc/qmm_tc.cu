@@ -13,27 +13,34 @@
 // D[128 x Mt] (fp32) lives in tensor memory.
 //
 // One CTA = one 128-row weight tile x one K range (split) x one chunk of at
-// most 256 x rows. Warp roles:
-//   warp 0      TMA producer of the packed-weight tiles (ring of kWStages)
-//   warp 1      TMA producer of the activation tiles (ring of kXStages),
-//               128-byte swizzled = the canonical K-major UMMA layout
+// most 256 x rows, one CTA per SM. The K range is walked in 256-column weight
+// stages, each split into two 128-column A stages (= activation stages).
+// Warp roles:
+//   warp 0      TMA producer of the packed-weight stages (ring of even depth)
+//   warp 1      TMA producer of the activation stages, 128-byte swizzled =
+//               the canonical K-major UMMA layout
 //   warps 2-3   MMA issuers: tcgen05.mma kind::f16, A operand from tensor
 //               memory, B operand (activations) from shared memory. The whole
 //               warp runs the issue loop (warp-uniform control flow) and
 //               elect.sync picks the lane that issues: a converged warp issues
-//               MMAs about twice as fast as one divergent lane. With two
-//               issuers, issuer h takes the K half h (one activation stage) of
-//               every weight stage into its own accumulator, so a stage's MMAs
-//               run on both at once; the epilogue adds the two accumulators in
-//               a fixed order.
-//   warps 4-19  dequantize: thread t of a warp in lane quadrant q owns weight
-//               row 32q + t and one 64-column quarter of the stage; it decodes
-//               the codes, computes w_hat = fma(q, s, b) in bf16x2/f16x2 (one
-//               rounding of the exact value) and stores the row slice straight
-//               into tensor memory with tcgen05.st (the A ring), so the
-//               weights never pass through shared memory a second time.
+//               MMAs about twice as fast as one divergent lane. Issuer j takes
+//               the A stages i == j (mod 2) into its own accumulator; the
+//               epilogue adds the two accumulators in a fixed order.
+//   warps 4-19  dequantize, as four groups of four warps (one warp per
+//               tensor-memory lane quadrant). Group g takes the A stages
+//               i == g (mod 4): thread t of the group's warp in quadrant q owns
+//               weight row 32q + t and decodes its 128 columns of the stage
+//               (one half of a weight stage), computes w_hat = fma(q, s, b) in
+//               bf16x2/f16x2 (one rounding of the exact value) and stores the
+//               row slice straight into tensor memory with tcgen05.st (the A
+//               ring of 64-column slots), so the weights never pass through
+//               shared memory a second time. The groups run on different
+//               stages, so they do not meet on one barrier per stage.
 //               After the K loop the same warps read the accumulator
 //               (tcgen05.ld) and write fp32 partials or the rounded output.
+// Every ring slot is always waited on by the same role, phase after phase
+// (mbarrier.try_wait.parity reports a phase two ahead as complete); the host
+// sizes the rings for that (even depths, at least four A slots).
 // Scales and biases of a stage arrive by TMA with its packed weights (same
 // barrier) when the row length K / group_size is a multiple of 8; otherwise
 // the dequantize warps read them from global memory. Keeping global loads out

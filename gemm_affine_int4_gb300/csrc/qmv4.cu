@@ -25,7 +25,8 @@
 //    two codes at mantissa bits 15..18 and 19..22, and one three-input logic
 //    op each (mask, then the exponent of 1.0f) gives the floats 1 + q/256 and
 //    1 + q/16 exactly. Per 32-bit word of 8 codes: 4 shifts, 8 logic ops and 8
-//    fmas, into an even-code and an odd-code accumulator that start at
+//    fmas (4 packed fma.rn.f32x2), into an even-code and an odd-code
+//    accumulator that start at
 //    -sum x_even and -sum x_odd of the chunk, so that
 //    256 * acc_even + 16 * acc_odd is the chunk's sum q x.
 #include <algorithm>
