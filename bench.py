@@ -182,6 +182,36 @@ def selected(only, fam, idx):
     return f == fam and (i == "" or int(i) == idx)
 
 
+# batched / strided qmm_t, measured beside the step (not part of it):
+# (batch, K, N, M): stacked weights [batch, N, K], activations a strided,
+# odd-offset view (rows K + 8 apart, one element in), so the call gathers them
+BATCHED_SHAPES = [(4, 4096, 4096, 16), (8, 2048, 2048, 22)]
+
+
+def batched_bytes(B, M, N, K):
+    return B * affine_bytes(M, N, K)
+
+
+def build_batched(torch, g4, dev, seed=7):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    bf = torch.bfloat16
+    out = []
+    for (B, K, N, M) in BATCHED_SHAPES:
+        w = torch.randn((B * N, K), generator=gen, device=dev, dtype=torch.float32) * 0.02
+        p, s, b = g4.gai4_quantize(w, BITS, GS, bf)
+        del w
+        p, s, b = p.view(B, N, -1), s.view(B, N, -1), b.view(B, N, -1)
+        base = torch.randn((B * M * (K + 8) + 16,), generator=gen, device=dev).to(bf)
+        x = torch.as_strided(base, (B, M, K), (M * (K + 8), K + 8, 1), 1)
+        ws_n = g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, BITS, GS, bf, 0)
+        ws = torch.empty(max(ws_n, 16) // 4 + 64, dtype=torch.float32, device=dev)
+        out.append(dict(kind="qmm_t_batched", p=p, s=s, b=b, x=x, out=torch.empty((B, M, N), dtype=bf, device=dev),
+                        ws=ws, B=B, M=M, N=N, K=K, bytes=batched_bytes(B, M, N, K)))
+    torch.cuda.synchronize()
+    return out
+
+
 def build_workload(torch, g4, dev, seed=0, only=None):
     """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
@@ -238,6 +268,9 @@ def issue(g4, c):
     elif k == "qmm_t":
         g4.gai4_qmm_t(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
                       workspace=c["ws"])
+    elif k == "qmm_t_batched":
+        g4.gai4_qmm_t_batched(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
+                              workspace=c["ws"])
     elif k == "q8_0":
         g4.gai4_q8_0_gemv(c["blocks"], c["x"], out=c["out"])
     else:
@@ -367,6 +400,11 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device status {st} after the timed region")
 
     per_call = None if args.no_per_call else time_per_call(torch, g4, calls, stream, fams)
+    # batched / strided qmm_t beside the step (same cold-L2 per-call timing)
+    extra = None
+    if not args.no_per_call and not args.only:
+        bcalls = build_batched(torch, g4, dev)
+        extra = time_per_call(torch, g4, {"qmm_t_batched": bcalls}, stream, ["qmm_t_batched"])
 
     # end to end through the public API: per step, H2D of every call's
     # activations from pinned host memory, the calls, D2H of every output
@@ -412,6 +450,7 @@ def run_gpu(args, rank, world, local_rank):
                      "avg_launch_us": round(dom_ms * 1e3 / n_launch, 3),
                      "traffic": None if traffic is None else round(traffic / n_launch)},
         "per_call_cold_l2": per_call,
+        "batched_cold_l2": extra,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,
@@ -422,6 +461,8 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def call_name(c):
+    if c["kind"] == "qmm_t_batched":
+        return f"qmm_t batched {c['B']}x (K{c['K']}xN{c['N']} M={c['M']}), strided odd-offset x"
     if c["kind"] == "qmm_t":
         return f"qmm_t K{c['K']}xN{c['N']} M={c['M']}"
     return f"{c['kind']} N{c['N']}xK{c['K']}"
@@ -466,10 +507,10 @@ def time_per_call(torch, g4, calls, stream, fams, reps=8):
             gbs = c["bytes"] / (us * 1e-6) / 1e9
             rec = {"call": call_name(c), "us": round(us, 3), "GB/s": round(gbs, 1),
                    "frac_of_hbm": round(gbs / hbm, 3)}
-            if c["kind"] == "qmm_t":
+            if c["kind"] in ("qmm_t", "qmm_t_batched"):
                 # min(HBM, tensor) roofline: the call cannot beat the larger of
                 # its byte time and its bf16 tensor-core time
-                flops = 2.0 * c["M"] * c["N"] * c["K"]
+                flops = 2.0 * c.get("B", 1) * c["M"] * c["N"] * c["K"]
                 roof_us = max(c["bytes"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
                 rec.update({"TFLOP/s": round(flops / (us * 1e-6) / 1e12, 2),
                             "frac_of_roofline": round(roof_us / us, 3)})

@@ -46,6 +46,9 @@ SIGNATURES = {
     "gai4_qmm_t_plan": ([_I64, _I64, _I64, _I, _I, _I, _I, ctypes.c_size_t, ctypes.POINTER(_I),
                          ctypes.POINTER(_I)], _I),
     "gai4_qmm_t_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I64, _I64, _I64, _I, _P], _I),
+    "gai4_qmm_t_batched": ([_P, _P, _P, _I, _P, _I64, _I64, _P, _I, _I, _I, _I64, _I64, _I64, _I64, _I, _P,
+                            ctypes.c_size_t, _P], _I),
+    "gai4_qmm_t_batched_workspace_bytes": ([_I64, _I64, _I64, _I64, _I, _I, _I, _I], ctypes.c_size_t),
     "gai4_q8_0_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_q4_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
@@ -84,6 +87,14 @@ def _ptr(t: torch.Tensor | None):
         raise ValueError("gai4: tensors must live on a CUDA device")
     if not t.is_contiguous():
         raise ValueError("gai4: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptr_strided(t: torch.Tensor):
+    """Device address of a strided view's first element (the strides travel
+    as separate arguments)."""
+    if not t.is_cuda:
+        raise ValueError("gai4: tensors must live on a CUDA device")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -185,6 +196,35 @@ def gai4_qmm_t(w_packed, scales, biases, x, out=None, bits: int = 4, group_size:
     _check("gai4_qmm_t", lib().gai4_qmm_t(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x), _ptr(out),
                                           _dtype(x), bits, group_size, M, N, K, split_k, _ptr(workspace),
                                           ws_bytes, _stream(stream)))
+    return out
+
+
+def gai4_qmm_t_batched_workspace_bytes(batch, M, N, K, bits, group_size, dtype, split_k=0) -> int:
+    return int(lib().gai4_qmm_t_batched_workspace_bytes(batch, M, N, K, bits, group_size, _DTYPE[dtype], split_k))
+
+
+def gai4_qmm_t_batched(w_packed, scales, biases, x, out=None, bits: int = 4, group_size: int = 64, split_k: int = 0,
+                       workspace=None, stream=None):
+    """out[b, m, n] = sum_k x[b, m, k] (s q + b)[e(b), n, k] for x [B, M, K]
+    (any batch / row strides, unit column stride, any element offset) and
+    weights [N, ...] (one matrix for every batch) or [B, N, ...] (stacked).
+    A workspace for the activation gather and the split-K partials is
+    allocated here when none is given."""
+    B, M, K = x.shape
+    if x.stride(2) != 1:
+        raise ValueError("gai4_qmm_t_batched: x needs unit column stride")
+    w_batched = 1 if w_packed.dim() == 3 else 0
+    N = w_packed.shape[-2]
+    if out is None:
+        out = torch.empty((B, M, N), dtype=x.dtype, device=x.device)
+    if workspace is None:
+        nbytes = gai4_qmm_t_batched_workspace_bytes(B, M, N, K, bits, group_size, x.dtype, split_k)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("gai4_qmm_t_batched",
+           lib().gai4_qmm_t_batched(_ptr(w_packed), _ptr(scales), _ptr(biases), w_batched, _ptr_strided(x), x.stride(0),
+                                    x.stride(1), _ptr(out), _dtype(x), bits, group_size, B, M, N, K, split_k,
+                                    _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -319,3 +319,68 @@ extern "C" gai4_status gai4_qmm_t_noalloc(const uint32_t* w_packed, const void* 
     return gai4_qmm_t(w_packed, scales, biases, x, out, dtype, bits, group_size, M, N, K, split_k, scratch,
                       (size_t)GAI4_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// ---------------------------------------------------------------------------
+// batched / strided qmm_t: gather the activations when they are not
+// contiguous rows on 16-byte boundaries, then one gai4_qmm_t per batch
+// ---------------------------------------------------------------------------
+namespace gai4 {
+static size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+static int dtype_bytes(gai4_dtype d) { return d == GAI4_F32 ? 4 : 2; }
+}  // namespace gai4
+
+extern "C" size_t gai4_qmm_t_batched_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K, int bits,
+                                                     int group_size, gai4_dtype dtype, int split_k) {
+    if (batch < 1 || M < 1 || K < 1) return 0;
+    return gai4::round256((size_t)batch * (size_t)M * (size_t)K * (size_t)gai4::dtype_bytes(dtype)) +
+           gai4_qmm_t_workspace_bytes(M, N, K, bits, group_size, dtype, split_k);
+}
+
+extern "C" gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* scales, const void* biases,
+                                          int w_batched, const void* x, int64_t x_batch_stride,
+                                          int64_t x_row_stride, void* out, gai4_dtype dtype, int bits,
+                                          int group_size, int64_t batch, int64_t M, int64_t N, int64_t K,
+                                          int split_k, void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace gai4;
+    if (batch < 1 || M < 1 || N < 1 || K < 1) return GAI4_ERR_INVALID_ARG;
+    if (!w_packed || !scales || !biases || !x || !out) return GAI4_ERR_INVALID_ARG;
+    if (x_row_stride < K || x_batch_stride < 0) return GAI4_ERR_INVALID_ARG;
+    if (dtype != GAI4_F32 && dtype != GAI4_F16 && dtype != GAI4_BF16) return GAI4_ERR_UNSUPPORTED;
+    if (bits < 1 || bits > 8 || group_size <= 0 || K % group_size != 0) return GAI4_ERR_INVALID_ARG;
+    const int tb = dtype_bytes(dtype);
+    if (((uintptr_t)x % (uintptr_t)tb) != 0 || ((uintptr_t)out % (uintptr_t)tb) != 0) return GAI4_ERR_MISALIGNED;
+    cudaStream_t s = (cudaStream_t)stream;
+    // weights of matrix e: w_packed + e * N * (K * bits / 32) words, scales and
+    // biases + e * N * (K / group_size) elements
+    const int64_t w_words = N * (K * bits / 32);
+    const int64_t sb_elems = N * (K / group_size);
+    const bool contiguous = x_row_stride == K && ((uintptr_t)x & 15u) == 0 &&
+                            (batch == 1 || ((x_batch_stride * tb) % 16) == 0);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    int64_t xbs = x_batch_stride;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    size_t ws_left = workspace ? workspace_bytes : 0;
+    if (!contiguous) {
+        const size_t need = round256((size_t)batch * (size_t)M * (size_t)K * (size_t)tb);
+        if (!workspace || workspace_bytes < need) return GAI4_ERR_WORKSPACE;
+        if (((uintptr_t)workspace & 15u) != 0) return GAI4_ERR_MISALIGNED;
+        cudaError_t e = launch_gather_rows(x, workspace, tb, batch, M, K, x_batch_stride, x_row_stride, s);
+        if (e != cudaSuccess) return GAI4_ERR_CUDA;
+        xb = ws;
+        xbs = M * K;
+        ws += need;
+        ws_left -= need;
+    }
+    for (int64_t b = 0; b < batch; ++b) {
+        const int64_t e = w_batched ? b : 0;
+        const uint32_t* wb = w_packed + e * w_words;
+        const uint8_t* sbp = static_cast<const uint8_t*>(scales) + (size_t)(e * sb_elems) * tb;
+        const uint8_t* bbp = static_cast<const uint8_t*>(biases) + (size_t)(e * sb_elems) * tb;
+        const void* xp = xb + (size_t)(b * xbs) * tb;
+        void* op = static_cast<uint8_t*>(out) + (size_t)(b * M * N) * tb;
+        const gai4_status st = gai4_qmm_t(wb, sbp, bbp, xp, op, dtype, bits, group_size, M, N, K, split_k,
+                                          ws_left ? ws : nullptr, ws_left, stream);
+        if (st != GAI4_OK) return st;
+    }
+    return GAI4_OK;
+}

@@ -84,6 +84,11 @@ cudaError_t launch_dequantize(const uint32_t* packed, const void* scales, const 
 cudaError_t launch_splitk_reduce(const float* partials, void* out, int64_t M, int64_t N,
                                  const SplitPlan& plan, int dtype, cudaStream_t s);
 
+// strided activations into contiguous rows (gather.cu):
+// dst[(b * M + m) * K + k] = src[b * batch_stride + m * row_stride + k]
+cudaError_t launch_gather_rows(const void* src, void* dst, int elem_bytes, int64_t B, int64_t M, int64_t K,
+                               int64_t batch_stride, int64_t row_stride, cudaStream_t s);
+
 // block-quantized GEMVs with TMA-staged rows (blockq_tma.cu): supported when
 // rows start on 16-byte boundaries and the activations fit in shared memory
 enum { BQ_Q8_0 = 0, BQ_Q4_K = 1 };

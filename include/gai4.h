@@ -148,6 +148,39 @@ gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group
                             int* path, int* splits);
 
 /*
+ * gai4_qmm_t_batched -- gai4_qmm_t over a batch of problems: 3-D stacked
+ * weights, strided and odd-offset activations (MLX PR, Correctness section,
+ * test_qmm_t_batched_and_strided; the Performance section's route copies
+ * activations at unaligned offsets before the matmul):
+ *   out[b, m, n] = sum_k x[b, m, k] * w_hat[e(b), n, k],   b < batch
+ *   e(b) = b when w_batched != 0: w_packed, scales and biases hold `batch`
+ *          matrices [N, ...] one after the other without gaps;
+ *   e(b) = 0 when w_batched == 0: one weight matrix serves every batch.
+ *   x: element (b, m, k) at x + b * x_batch_stride + m * x_row_stride + k,
+ *      strides in elements of T (x_batch_stride >= 0, x_row_stride >= K); x
+ *      need only be aligned to its element size.
+ *   out [batch, M, N] T, contiguous.
+ * When the activations are not contiguous rows on 16-byte boundaries, one
+ * copy kernel first gathers them into `workspace` ([batch, M, K] T); every
+ * batch then runs as gai4_qmm_t, in stream order, with the rest of the
+ * workspace for its split-K partials (split_k as for gai4_qmm_t).
+ * workspace: device, 16-byte aligned, workspace_bytes >=
+ * gai4_qmm_t_batched_workspace_bytes(...) (NULL allowed when that is 0).
+ * Errors: as gai4_qmm_t for each batch's arguments (the first failing batch
+ * stops the call); GAI4_ERR_INVALID_ARG for batch < 1 or bad strides;
+ * GAI4_ERR_WORKSPACE when a gather is needed and the workspace is too small.
+ */
+gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* scales, const void* biases, int w_batched,
+                               const void* x, int64_t x_batch_stride, int64_t x_row_stride, void* out,
+                               gai4_dtype dtype, int bits, int group_size, int64_t batch, int64_t M, int64_t N,
+                               int64_t K, int split_k, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace gai4_qmm_t_batched may need: the gathered activations (rounded up
+ * to 256 bytes) plus gai4_qmm_t_workspace_bytes(M, N, K, ...) for the splits. */
+size_t gai4_qmm_t_batched_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K, int bits,
+                                          int group_size, gai4_dtype dtype, int split_k);
+
+/*
  * gai4_qmm_t_noalloc -- gai4_qmm_t for callers that cannot allocate device
  * memory. (No counterpart on the pages; an addition of this library.)
  *

@@ -104,3 +104,29 @@ def test_binding_requires_cuda_tensors(lib):
     with pytest.raises(ValueError):
         g4.gai4_qmv(torch.zeros(4, 8, dtype=torch.int32), torch.zeros(4, 1), torch.zeros(4, 1), torch.zeros(64),
                     bits=4, group_size=64)
+
+
+def test_batched_rejects_bad_arguments_without_launching(lib):
+    A = _fake()
+    f = lib.gai4_qmm_t_batched
+    # (w, s, b, w_batched, x, x_batch_stride, x_row_stride, out, dtype, bits, gs, batch, M, N, K, split_k, ws, bytes, stream)
+    assert f(A, A, A, 1, A, 256 * 8, 256, A, 2, 4, 64, 0, 8, 128, 256, 0, None, 0, None) == g4.GAI4_ERR_INVALID_ARG
+    assert f(A, A, A, 1, None, 256 * 8, 256, A, 2, 4, 64, 2, 8, 128, 256, 0, None, 0, None) == g4.GAI4_ERR_INVALID_ARG
+    # a row stride shorter than a row
+    assert f(A, A, A, 1, A, 256 * 8, 255, A, 2, 4, 64, 2, 8, 128, 256, 0, None, 0, None) == g4.GAI4_ERR_INVALID_ARG
+    # activations not aligned to their element size
+    assert f(A, A, A, 1, _fake(0x10001), 256 * 8, 256, A, 2, 4, 64, 2, 8, 128, 256, 0, None, 0,
+             None) == g4.GAI4_ERR_MISALIGNED
+    # strided (or odd-offset) activations need the gather buffer in the workspace
+    assert f(A, A, A, 1, A, 264 * 8, 264, A, 2, 4, 64, 2, 8, 128, 256, 0, None, 0, None) == g4.GAI4_ERR_WORKSPACE
+    assert f(A, A, A, 1, _fake(0x10002), 256 * 8, 256, A, 2, 4, 64, 2, 8, 128, 256, 0, A, 1024,
+             None) == g4.GAI4_ERR_WORKSPACE
+
+
+def test_batched_workspace_bytes(lib):
+    import torch
+    # gather buffer (rounded up to 256 bytes) + the split-K partials of one batch
+    got = g4.gai4_qmm_t_batched_workspace_bytes(3, 33, 4096, 14336, 4, 64, torch.bfloat16, 0)
+    gather = (3 * 33 * 14336 * 2 + 255) // 256 * 256
+    assert got == gather + g4.gai4_qmm_t_workspace_bytes(33, 4096, 14336, 4, 64, torch.bfloat16, 0)
+    assert g4.gai4_qmm_t_batched_workspace_bytes(0, 33, 4096, 14336, 4, 64, torch.bfloat16, 0) == 0
