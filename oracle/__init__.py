@@ -63,6 +63,10 @@ def lib():
         L.orc_q4_k_scale_min.restype = None
         L.orc_q4_k_dequant_block.argtypes = [P, P]
         L.orc_q4_k_gemv.argtypes = [P, P, I64, I64, P, I64, P, P]
+        L.orc_quantize_x_q8.argtypes = [P, I64, P, P]
+        L.orc_q8_0_block_dot_i8.argtypes = [P, P]
+        L.orc_q8_0_block_dot_i8.restype = ctypes.c_int64
+        L.orc_q8_0_gemv_i8.argtypes = [P, P, P, I64, I64, P, I64, P, P]
         for name in ("orc_unpack", "orc_pack", "orc_quantize", "orc_dequantize", "orc_qmm",
                      "orc_q8_0_dequant_block", "orc_q8_0_gemv", "orc_q4_k_dequant_block",
                      "orc_q4_k_gemv"):
@@ -207,6 +211,40 @@ def q8_0_gemv(blocks: np.ndarray, x: np.ndarray, rows=None):
     absdot = np.zeros(nr, dtype=np.float64)
     _check(lib().orc_q8_0_gemv(_p(blocks), _p(x), N, K, _p(r), nr, _p(out), _p(absdot)),
            "q8_0_gemv")
+    return out, absdot
+
+
+def quantize_x_q8(x: np.ndarray):
+    """x f32 [K] (K % 32 == 0) -> (xq int8 [K], xd f32 [K/32]): per 32-element
+    block d = amax / 127 and q = rint(x / d) in binary32 (q = 0 when d = 0)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    K = x.shape[0]
+    xq = np.zeros(K, dtype=np.int8)
+    xd = np.zeros(K // 32, dtype=np.float32)
+    _check(lib().orc_quantize_x_q8(_p(x), K, _p(xq), _p(xd)), "quantize_x_q8")
+    return xq, xd
+
+
+def q8_0_block_dot_i8(block9: np.ndarray, xq32: np.ndarray) -> int:
+    b = np.ascontiguousarray(block9, dtype=np.uint32).reshape(9)
+    q = np.ascontiguousarray(xq32, dtype=np.int8).reshape(32)
+    return int(lib().orc_q8_0_block_dot_i8(_p(b), _p(q)))
+
+
+def q8_0_gemv_i8(blocks: np.ndarray, xq: np.ndarray, xd: np.ndarray, rows=None):
+    """blocks u32 [N, K/32, 9], xq int8 [K], xd f32 [K/32] -> (out f64, absdot f64):
+    out[n] = sum_b d_w[n, b] * xd[b] * (exact integer dot of the block's codes)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint32)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xd = np.ascontiguousarray(xd, dtype=np.float32)
+    N = blocks.shape[0]
+    K = xq.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros(nr, dtype=np.float64)
+    absdot = np.zeros(nr, dtype=np.float64)
+    _check(lib().orc_q8_0_gemv_i8(_p(blocks), _p(xq), _p(xd), N, K, _p(r), nr, _p(out), _p(absdot)),
+           "q8_0_gemv_i8")
     return out, absdot
 
 

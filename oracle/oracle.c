@@ -26,6 +26,8 @@
  *    Correctness section: fp32 accumulation, one rounding after the sum;
  *    its reproduction script: quantize(w, group_size=64, bits=4) and
  *    quantized_matmul(x, wq, scales, biases, transpose=True).
+ *  - hanzo-kernel quant.rs, dp4a matvecs: int8 activations, exact integer
+ *    inner sums (orc_quantize_x_q8, orc_q8_0_gemv_i8).
  *  - hanzo-kernel quant.rs: Q8_0 (one f16 scale + 32 int8 per block; packed
  *    9-word block, scale in the low half of word 0), Q4_K (144-byte super-block
  *    d, dmin, scales[12], qs[128]; get_scale_min_k4; w = d*sc*q - dmin*m).
@@ -345,6 +347,84 @@ int orc_q8_0_gemv(const uint32_t* blocks, const float* x, int64_t N, int64_t K,
                 acc += p;
                 aacc += fabs(p);
             }
+        }
+        out[j] = acc;
+        if (absdot) absdot[j] = aacc;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q8_0 with integer activations (hanzo-kernel quant.rs, "dp4a matvec" and    */
+/* "PACKED dp4a matvec": int8 weights and int8 activations, the inner sum an  */
+/* exact integer dot product, then out[row] = sum_block wd * dot(qw, xq)).     */
+/* The activations are quantized per 32-element block: d = amax / 127 and    */
+/* q = rint(x / d), both in binary32 (the codes a binary32 implementation     */
+/* must produce), q = 0 for an all-zero block; the block's activation scale   */
+/* multiplies the weight scale.                                              */
+/* ------------------------------------------------------------------------ */
+
+int orc_quantize_x_q8(const float* x, int64_t K, int8_t* xq, float* xd)
+{
+    if (K <= 0 || K % 32) return ORC_EINVAL;
+    for (int64_t b = 0; b < K / 32; ++b) {
+        const float* xb = x + 32 * b;
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float a = fabsf(xb[i]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        xd[b] = d;
+        for (int i = 0; i < 32; ++i) {
+            int q = 0;
+            if (d != 0.0f) {
+                float r = rintf(xb[i] / d);
+                q = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+            }
+            xq[32 * b + i] = (int8_t)q;
+        }
+    }
+    return ORC_OK;
+}
+
+/* the exact integer dot product of one Q8_0 block's codes with 32 int8 codes */
+int64_t orc_q8_0_block_dot_i8(const uint32_t* blk, const int8_t* xq32)
+{
+    int64_t s = 0;
+    for (int j = 0; j < 32; ++j) {
+        unsigned byte = (blk[1 + j / 4] >> (8 * (j % 4))) & 0xffu;
+        int q = byte >= 128 ? (int)byte - 256 : (int)byte;
+        s += (int64_t)q * (int64_t)xq32[j];
+    }
+    return s;
+}
+
+/* out[j] = sum_b d_w[rows[j], b] * xd[b] * dot_b (binary64; dot_b exact) */
+int orc_q8_0_gemv_i8(const uint32_t* blocks, const int8_t* xq, const float* xd, int64_t N, int64_t K,
+                     const int64_t* rows, int64_t nrows, double* out, double* absdot)
+{
+    if (N < 0 || K <= 0 || K % 32) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t nb = K / 32;
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) return ORC_EINVAL;
+        double acc = 0.0, aacc = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint32_t* blk = blocks + (n * nb + b) * 9;
+            double dw = orc_f16_to_f64((uint16_t)(blk[0] & 0xffffu));
+            double scale = dw * (double)xd[b];
+            int64_t dot = orc_q8_0_block_dot_i8(blk, xq + 32 * b);
+            int64_t adot = 0;
+            for (int i = 0; i < 32; ++i) {
+                unsigned byte = (blk[1 + i / 4] >> (8 * (i % 4))) & 0xffu;
+                int q = byte >= 128 ? (int)byte - 256 : (int)byte;
+                int64_t p = (int64_t)q * (int64_t)xq[32 * b + i];
+                adot += p < 0 ? -p : p;
+            }
+            acc += scale * (double)dot;
+            aacc += fabs(scale) * (double)adot;
         }
         out[j] = acc;
         if (absdot) absdot[j] = aacc;

@@ -371,3 +371,86 @@ def test_oracle_rejects_bad_shapes():
         oracle.quantize(np.zeros((2, 64), np.float32), 5, 64, "bf16")   # unsupported width
     with pytest.raises(ValueError):
         oracle.q4_k_gemv(np.zeros((1, 1, 144), np.uint8), np.zeros(100, np.float32))
+
+
+# --- Q8_0 with integer activations (hanzo-kernel quant.rs, dp4a matvecs) -------
+
+def test_quantize_x_q8_invariants():
+    """Per 32-element block: |q| <= 127, the largest |x| maps to +-127, every
+    element is within d/2 of d*q, and an all-zero block gives q = 0, d = 0."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(32 * 6).astype(np.float32) * np.float32(3.0)
+    x[32:64] = 0.0                      # an all-zero block
+    x[64:96] = 0.0
+    x[70] = np.float32(-0.75)           # a block with one non-zero element
+    xq, xd = oracle.quantize_x_q8(x)
+    for b in range(6):
+        xb, qb, d = x[32 * b:32 * b + 32], xq[32 * b:32 * b + 32].astype(np.int64), float(xd[b])
+        assert np.all(np.abs(qb) <= 127)
+        if b == 1:
+            assert d == 0.0 and np.all(qb == 0)
+            continue
+        i = int(np.argmax(np.abs(xb)))
+        assert abs(int(qb[i])) == 127 and np.sign(qb[i]) == np.sign(xb[i])
+        err = np.abs(xb.astype(np.float64) - d * qb)
+        assert np.all(err <= d / 2 * (1 + 2.0 ** -20)), (b, err.max(), d)
+    assert xq[70] == -127 and np.count_nonzero(xq[64:96]) == 1
+
+
+def test_q8_0_block_dot_i8_brute_force():
+    """The integer dot against a second decoding route: the 8 code words
+    viewed as 32 little-endian signed bytes, summed with Python integers."""
+    rng = np.random.default_rng(6)
+    blocks = synth.q8_0_blocks(4, 32 * 5, 7)
+    for n in range(4):
+        for b in range(5):
+            blk = blocks[n, b]
+            xq = rng.integers(-128, 128, size=32).astype(np.int8)
+            codes = np.frombuffer(blk[1:9].astype("<u4").tobytes(), dtype=np.int8)
+            want = sum(int(c) * int(v) for c, v in zip(codes, xq))
+            assert oracle.q8_0_block_dot_i8(blk, xq) == want
+
+
+def test_q8_0_gemv_i8_exact_rational():
+    """Tiny case in exact rational arithmetic: d_w (f16), xd (f32) and the
+    integer dots are exact rationals; the oracle's binary64 sum is within a few
+    ulps of the exact value."""
+    from fractions import Fraction
+    N, K = 3, 96
+    blocks = synth.q8_0_blocks(N, K, 11)
+    x = synth.f32_vector(K, 12)
+    xq, xd = oracle.quantize_x_q8(x)
+    got, _ = oracle.q8_0_gemv_i8(blocks, xq, xd)
+    for n in range(N):
+        total = Fraction(0)
+        for b in range(K // 32):
+            blk = blocks[n, b]
+            dw = Fraction(float(np.array([blk[0] & 0xFFFF], dtype=np.uint16).view(np.float16)[0]))
+            codes = np.frombuffer(blk[1:9].astype("<u4").tobytes(), dtype=np.int8)
+            dot = sum(int(c) * int(v) for c, v in zip(codes, xq[32 * b:32 * b + 32]))
+            total += dw * Fraction(float(xd[b])) * dot
+        assert abs(got[n] - float(total)) <= 8 * np.spacing(abs(float(total))) + 1e-300
+
+
+def test_q8_0_gemv_i8_agrees_with_the_float_path():
+    """Against the a7 oracle on the dequantized activations x = xd * xq (f32):
+    the two differ only by the f32 rounding of xd * xq."""
+    N, K = 7, 32 * 12
+    blocks = synth.q8_0_blocks(N, K, 21)
+    xq, xd = oracle.quantize_x_q8(synth.f32_vector(K, 22))
+    x_deq = (xq.astype(np.float32).reshape(-1, 32) * xd[:, None]).reshape(-1)
+    a, absdot = oracle.q8_0_gemv_i8(blocks, xq, xd)
+    b, _ = oracle.q8_0_gemv(blocks, x_deq)
+    assert np.all(np.abs(a - b) <= 2.0 ** -22 * absdot)
+
+
+def test_q8_0_gemv_i8_closed_form():
+    """q_w = 1 and q_x = 1 everywhere: out[n] = 32 * sum_b d_w[n, b] * xd[b]."""
+    N, K = 4, 32 * 3
+    blocks = synth.q8_0_blocks(N, K, 31)
+    blocks[:, :, 1:] = 0x01010101
+    xq = np.ones(K, dtype=np.int8)
+    xd = np.array([0.5, 0.25, 2.0], dtype=np.float32)
+    got, _ = oracle.q8_0_gemv_i8(blocks, xq, xd)
+    dw = (blocks[:, :, 0] & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(got, 32 * (dw * xd.astype(np.float64)).sum(axis=1))
