@@ -212,6 +212,23 @@ def build_batched(torch, g4, dev, seed=7):
     return out
 
 
+def q8_i8_bytes(N, K):
+    return N * (K // 32) * 36 + K + (K // 32) * 4 + N * 4
+
+
+def build_q8_i8(torch, g4, dev):
+    """Q8_0 with integer activations (x quantized on the GPU once, outside the timing)."""
+    import synth
+    out = []
+    for i, (N, K) in enumerate(BLOCKQ_SHAPES):
+        blk = torch.from_numpy(synth.q8_0_blocks(N, K, 300 + i).view(np.int32)).to(dev)
+        xq, xd = g4.gai4_quantize_x_q8(torch.from_numpy(synth.f32_vector(K, 301 + i)).to(dev))
+        out.append(dict(kind="q8_0_i8", blocks=blk, xq=xq, xd=xd, out=torch.empty(N, device=dev), N=N, K=K,
+                        bytes=q8_i8_bytes(N, K)))
+    torch.cuda.synchronize()
+    return out
+
+
 def build_workload(torch, g4, dev, seed=0, only=None):
     """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
@@ -271,6 +288,8 @@ def issue(g4, c):
     elif k == "qmm_t_batched":
         g4.gai4_qmm_t_batched(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
                               workspace=c["ws"])
+    elif k == "q8_0_i8":
+        g4.gai4_q8_0_gemv_i8(c["blocks"], c["xq"], c["xd"], out=c["out"])
     elif k == "q8_0":
         g4.gai4_q8_0_gemv(c["blocks"], c["x"], out=c["out"])
     else:
@@ -401,10 +420,12 @@ def run_gpu(args, rank, world, local_rank):
 
     per_call = None if args.no_per_call else time_per_call(torch, g4, calls, stream, fams)
     # batched / strided qmm_t beside the step (same cold-L2 per-call timing)
-    extra = None
+    extra = extra_i8 = None
     if not args.no_per_call and not args.only:
         bcalls = build_batched(torch, g4, dev)
         extra = time_per_call(torch, g4, {"qmm_t_batched": bcalls}, stream, ["qmm_t_batched"])
+        icalls = build_q8_i8(torch, g4, dev)
+        extra_i8 = time_per_call(torch, g4, {"q8_0_i8": icalls}, stream, ["q8_0_i8"])
 
     # end to end through the public API: per step, H2D of every call's
     # activations from pinned host memory, the calls, D2H of every output
@@ -451,6 +472,7 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": None if traffic is None else round(traffic / n_launch)},
         "per_call_cold_l2": per_call,
         "batched_cold_l2": extra,
+        "q8_0_int8_activations_cold_l2": extra_i8,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,
@@ -461,6 +483,8 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def call_name(c):
+    if c["kind"] == "q8_0_i8":
+        return f"q8_0 int8 activations N{c['N']}xK{c['K']}"
     if c["kind"] == "qmm_t_batched":
         return f"qmm_t batched {c['B']}x (K{c['K']}xN{c['N']} M={c['M']}), strided odd-offset x"
     if c["kind"] == "qmm_t":

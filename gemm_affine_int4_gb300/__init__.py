@@ -51,6 +51,8 @@ SIGNATURES = {
     "gai4_qmm_t_batched_workspace_bytes": ([_I64, _I64, _I64, _I64, _I, _I, _I, _I], ctypes.c_size_t),
     "gai4_q8_0_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_q4_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
+    "gai4_quantize_x_q8": ([_P, _P, _P, _I64, _P], _I),
+    "gai4_q8_0_gemv_i8": ([_P, _P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
 }
 
@@ -252,6 +254,30 @@ def gai4_q8_0_gemv(blocks, x, out=None, stream=None):
     if out is None:
         out = torch.empty((N,), dtype=torch.float32, device=x.device)
     _check("gai4_q8_0_gemv", lib().gai4_q8_0_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
+    return out
+
+
+def gai4_quantize_x_q8(x, xq=None, xd=None, stream=None):
+    """x [K] float32 -> (xq [K] int8, xd [K/32] float32): per 32-element
+    block d = amax / 127, q = rint(x / d) clamped to +-127."""
+    K = x.shape[-1]
+    if xq is None:
+        xq = torch.empty(K, dtype=torch.int8, device=x.device)
+    if xd is None:
+        xd = torch.empty(K // 32, dtype=torch.float32, device=x.device)
+    _check("gai4_quantize_x_q8", lib().gai4_quantize_x_q8(_ptr(x), _ptr(xq), _ptr(xd), K, _stream(stream)))
+    return xq, xd
+
+
+def gai4_q8_0_gemv_i8(blocks, xq, xd, out=None, stream=None):
+    """blocks [N, K/32, 9] int32/uint32, xq [K] int8, xd [K/32] float32 ->
+    out [N] float32 (block dots exact in integers)."""
+    N = blocks.shape[0]
+    K = xq.shape[-1]
+    if out is None:
+        out = torch.empty(N, dtype=torch.float32, device=xq.device)
+    _check("gai4_q8_0_gemv_i8", lib().gai4_q8_0_gemv_i8(_ptr(blocks), _ptr(xq), _ptr(xd), _ptr(out), N, K,
+                                                        _stream(stream)))
     return out
 
 

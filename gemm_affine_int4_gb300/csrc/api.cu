@@ -273,6 +273,24 @@ gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, in
     return from_cuda(launch_q4_k_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
 }
 
+gai4_status gai4_quantize_x_q8(const float* x, int8_t* xq, float* xd, int64_t K, void* stream) {
+    if (!x || !xq || !xd || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || ((uintptr_t)xd & 3u) != 0) return GAI4_ERR_MISALIGNED;
+    return from_cuda(launch_quantize_x_q8(x, xq, xd, K, (cudaStream_t)stream));
+}
+
+gai4_status gai4_q8_0_gemv_i8(const uint32_t* blocks, const int8_t* xq, const float* xd, float* out, int64_t N,
+                              int64_t K, void* stream) {
+    if (!blocks || !xq || !xd || !out || N <= 0 || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!aligned16(blocks) || !aligned16(xq) || ((uintptr_t)xd & 3u) != 0) return GAI4_ERR_MISALIGNED;
+    if (bq_tma_supported(BQ_Q8_0_I8, N, K, blocks, xq)) {
+        int* st = status_ptr();
+        if (!st) return GAI4_ERR_CUDA;
+        return from_cuda(launch_q8_0_i8_gemv_tma(blocks, xq, xd, out, N, K, st, 2000000000LL, (cudaStream_t)stream));
+    }
+    return from_cuda(launch_q8_0_i8_gemv(blocks, xq, xd, out, N, K, (cudaStream_t)stream));
+}
+
 gai4_status gai4_last_device_status(void* stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GAI4_ERR_CUDA;
     int v = 0;

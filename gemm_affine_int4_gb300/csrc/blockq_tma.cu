@@ -63,7 +63,9 @@ struct BqArgs {
     int n_groups;          // row groups = ceil(N / (kR G))
     uint32_t stage_bytes;  // C * kR * G * 1152
     uint32_t x_off, sum_off, pend_off, bar_off;   // shared-memory layout
-    const float* x;
+    const float* x;        // binary32 activations (Q8_0, Q4_K)
+    const int8_t* xq;      // int8 activations and their per-block scales (Q8_0 with integer activations)
+    const float* xd;
     float* out;
     int K;
     int last_half;         // Q4_K: the last chunk holds at most 4 super-blocks
@@ -149,6 +151,19 @@ template <int FMT>
 __device__ void stage_x(const BqArgs& a, uint8_t* smem) {
     float4* xs = reinterpret_cast<float4*>(smem + a.x_off);
     float* sums = reinterpret_cast<float*>(smem + a.sum_off);
+    if constexpr (FMT == BQ_Q8_0_I8) {
+        // chunk ch, block b (lane), half j: 16 code bytes at uint4 index
+        // (ch * 2 + j) * 32 + b; sums[32 ch + b] = the block's activation scale
+        uint4* xs4 = reinterpret_cast<uint4*>(smem + a.x_off);
+        const int nblk = a.K / 32;
+        for (int p = threadIdx.x; p < a.chunks * 64; p += kCW * 32) {
+            const int ch = p >> 6, j = (p >> 5) & 1, b = p & 31, g = ch * 32 + b;
+            xs4[(ch * 2 + j) * 32 + b] =
+                g < nblk ? *reinterpret_cast<const uint4*>(a.xq + 32 * (int64_t)g + 16 * j) : make_uint4(0, 0, 0, 0);
+        }
+        for (int r = threadIdx.x; r < a.chunks * 32; r += kCW * 32) sums[r] = r < nblk ? a.xd[r] : 0.f;
+        return;
+    }
     const int total = a.chunks * 128;   // a multiple of 32: whole warps in the shuffles
     for (int v = threadIdx.x; v < total; v += kCW * 32) {
         const int c = v >> 2, qq = v & 3;   // run (Q8_0 block) or item (Q4_K), quarter
@@ -306,7 +321,24 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
             for (int c = 0; c < n; ++c) {
                 const uint32_t rows = st + (uint32_t)c * (uint32_t)RS * kChunkBytes;   // row kR * wg of chunk c
                 const int ch = c0 + c;
-                if constexpr (FMT == BQ_Q8_0) {
+                if constexpr (FMT == BQ_Q8_0_I8) {
+                    // block `lane`: its 32 activation codes (two 16-byte pieces),
+                    // then per row the exact integer dot of the codes (dp4a)
+                    const uint32_t xp = xs_base + (uint32_t)(ch * 2 * 32 + lane) * 16u;
+                    const uint4 xa = lds128(xp), xb = lds128(xp + 32u * 16u);
+                    const int xw[8] = {(int)xa.x, (int)xa.y, (int)xa.z, (int)xa.w,
+                                       (int)xb.x, (int)xb.y, (int)xb.z, (int)xb.w};
+                    const float dx = sums[ch * 32 + lane];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+                        const uint32_t bp = rows + (uint32_t)r * kChunkBytes + 36u * (uint32_t)lane;
+                        const uint32_t hdr = lds32(bp);
+                        int dot = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dot = __dp4a((int)lds32(bp + 4u + 4u * (uint32_t)i), xw[i], dot);
+                        part[r] = fmaf(f16_bits_to_f32(hdr) * dx, (float)dot, part[r]);   // |dot| < 2^24: exact
+                    }
+                } else if constexpr (FMT == BQ_Q8_0) {
                     // block `lane` of the chunk: 9 words at 36 * lane (odd word
                     // stride: no bank conflicts)
                     const uint32_t xp = xs_base + (uint32_t)(ch * 8 * 32 + lane) * 16u;
@@ -466,6 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1) q8_0_tma_kernel(const __grid_cons
 __global__ void __launch_bounds__(kThreads, 1) q4_k_tma_kernel(const __grid_constant__ CUtensorMap wmap, const BqArgs a) {
     bq_tma_body<BQ_Q4_K>(wmap, a);
 }
+__global__ void __launch_bounds__(kThreads, 1) q8_0_i8_tma_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                  const BqArgs a) {
+    bq_tma_body<BQ_Q8_0_I8>(wmap, a);
+}
 
 int num_sms_cached() {
     static int sms = 0;
@@ -498,8 +534,8 @@ bool plan_bq(int64_t N, int chunks, int K, int fmt, BqArgs& a, size_t& smem) {
     a.last_half = fmt == BQ_Q4_K && sb_last != 0 && sb_last <= 4;
     a.n_groups = (int)((N + kR * a.G - 1) / (kR * a.G));
     a.stage_bytes = (uint32_t)a.C * (uint32_t)(kR * a.G) * kChunkBytes;
-    const size_t x_bytes = (size_t)chunks * (fmt == BQ_Q8_0 ? 1024 : 2048) * 4;
-    const size_t sum_bytes = (size_t)chunks * 32 * (fmt == BQ_Q8_0 ? 1 : 2) * 4;
+    const size_t x_bytes = (size_t)chunks * (fmt == BQ_Q4_K ? 2048 * 4 : (fmt == BQ_Q8_0 ? 1024 * 4 : 1024));
+    const size_t sum_bytes = (size_t)chunks * 32 * (fmt == BQ_Q4_K ? 2 : 1) * 4;
     const size_t pend_bytes = (size_t)2 * kFlush * kCW * kR * 4;
     const size_t bar_bytes = 2 * kMaxDepth * 8 + 16;
     const size_t fixed = 128 + x_bytes + sum_bytes + pend_bytes + bar_bytes;
@@ -525,8 +561,8 @@ bool plan_bq(int64_t N, int chunks, int K, int fmt, BqArgs& a, size_t& smem) {
 }
 
 template <int FMT>
-cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N, int64_t K, size_t row_bytes,
-                      int* status, long long spin_limit, cudaStream_t stream) {
+cudaError_t launch_bq(const void* blocks, const float* x, const int8_t* xq, const float* xd, float* out, int64_t N,
+                      int64_t K, size_t row_bytes, int* status, long long spin_limit, cudaStream_t stream) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int chunks = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
@@ -543,16 +579,18 @@ cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     a.x = x;
+    a.xq = xq;
+    a.xd = xd;
     a.out = out;
     a.status = status;
     a.spin_limit = spin_limit;
     if (!a.status) return cudaErrorInvalidValue;
     using KernFn = void (*)(const CUtensorMap, const BqArgs);
-    const KernFn kern = FMT == BQ_Q8_0 ? q8_0_tma_kernel : q4_k_tma_kernel;
-    static unsigned long long configured = 0ull;   // bit (2 * device + format)
+    const KernFn kern = FMT == BQ_Q8_0 ? q8_0_tma_kernel : (FMT == BQ_Q4_K ? q4_k_tma_kernel : q8_0_i8_tma_kernel);
+    static unsigned long long configured = 0ull;   // bit (3 * device + format)
     int dev = 0;
     cudaGetDevice(&dev);
-    const int bit = 2 * dev + FMT;
+    const int bit = 3 * dev + FMT;
     if (bit >= 64 || !(configured & (1ull << bit))) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
@@ -566,10 +604,10 @@ cudaError_t launch_bq(const void* blocks, const float* x, float* out, int64_t N,
 
 // Rows must start on 16-byte boundaries (TMA) and the staged activations must
 // fit in shared memory next to a ring of at least two stages per set.
-bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const float* x) {
+bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const void* x) {
     if (N <= 0 || N > (int64_t)1 << 30 || K <= 0 || K > (int64_t)1 << 20) return false;
     if (((uintptr_t)blocks & 15u) || ((uintptr_t)x & 15u)) return false;
-    const size_t row_bytes = fmt == BQ_Q8_0 ? (size_t)K / 32 * 36 : (size_t)K / 256 * 144;
+    const size_t row_bytes = fmt == BQ_Q4_K ? (size_t)K / 256 * 144 : (size_t)K / 32 * 36;
     if (row_bytes % 16 != 0) return false;
     if (!encode_fn()) return false;
     BqArgs a;
@@ -580,11 +618,15 @@ bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const f
 
 cudaError_t launch_q8_0_gemv_tma(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                                  int* status, long long spin_limit, cudaStream_t s) {
-    return launch_bq<BQ_Q8_0>(blocks, x, out, N, K, (size_t)K / 32 * 36, status, spin_limit, s);
+    return launch_bq<BQ_Q8_0>(blocks, x, nullptr, nullptr, out, N, K, (size_t)K / 32 * 36, status, spin_limit, s);
 }
 cudaError_t launch_q4_k_gemv_tma(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                                  int* status, long long spin_limit, cudaStream_t s) {
-    return launch_bq<BQ_Q4_K>(blocks, x, out, N, K, (size_t)K / 256 * 144, status, spin_limit, s);
+    return launch_bq<BQ_Q4_K>(blocks, x, nullptr, nullptr, out, N, K, (size_t)K / 256 * 144, status, spin_limit, s);
+}
+cudaError_t launch_q8_0_i8_gemv_tma(const uint32_t* blocks, const int8_t* xq, const float* xd, float* out, int64_t N,
+                                    int64_t K, int* status, long long spin_limit, cudaStream_t s) {
+    return launch_bq<BQ_Q8_0_I8>(blocks, nullptr, xq, xd, out, N, K, (size_t)K / 32 * 36, status, spin_limit, s);
 }
 
 }  // namespace gai4

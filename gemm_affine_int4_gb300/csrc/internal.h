@@ -91,12 +91,19 @@ cudaError_t launch_gather_rows(const void* src, void* dst, int elem_bytes, int64
 
 // block-quantized GEMVs with TMA-staged rows (blockq_tma.cu): supported when
 // rows start on 16-byte boundaries and the activations fit in shared memory
-enum { BQ_Q8_0 = 0, BQ_Q4_K = 1 };
-bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const float* x);
+enum { BQ_Q8_0 = 0, BQ_Q4_K = 1, BQ_Q8_0_I8 = 2 };
+bool bq_tma_supported(int fmt, int64_t N, int64_t K, const void* blocks, const void* x);
 cudaError_t launch_q8_0_gemv_tma(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                                  int* status, long long spin_limit, cudaStream_t s);
 cudaError_t launch_q4_k_gemv_tma(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                                  int* status, long long spin_limit, cudaStream_t s);
+cudaError_t launch_q8_0_i8_gemv_tma(const uint32_t* blocks, const int8_t* xq, const float* xd, float* out, int64_t N,
+                                    int64_t K, int* status, long long spin_limit, cudaStream_t s);
+
+// Q8_0 with integer activations, general case, and the activation quantizer (q8_act.cu)
+cudaError_t launch_q8_0_i8_gemv(const uint32_t* blocks, const int8_t* xq, const float* xd, float* out, int64_t N,
+                                int64_t K, cudaStream_t s);
+cudaError_t launch_quantize_x_q8(const float* x, int8_t* xq, float* xd, int64_t K, cudaStream_t s);
 
 // block-quantized GEMVs, general case (blockq.cu)
 cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N,

@@ -223,6 +223,28 @@ gai4_status gai4_q8_0_gemv(const uint32_t* blocks, const float* x, float* out,
                            int64_t N, int64_t K, void* stream);
 
 /*
+ * gai4_quantize_x_q8 -- int8 activations for gai4_q8_0_gemv_i8 (hanzo-kernel
+ * quant.rs, dp4a matvecs: "integer activations (xq) so the int dot is
+ * exact"). Per 32-element block b of x [K] float32:
+ *   xd[b] = amax_b / 127,  xq[32b + i] = clamp(rint(x[32b + i] / xd[b]), -127, 127)
+ * in binary32 (IEEE division, round to nearest even); xq = 0 when xd[b] = 0.
+ * K a multiple of 32; x and xq 16-byte aligned, xd 4-byte aligned.
+ */
+gai4_status gai4_quantize_x_q8(const float* x, int8_t* xq, float* xd, int64_t K, void* stream);
+
+/*
+ * gai4_q8_0_gemv_i8 -- Q8_0 matrix-vector product with integer activations
+ * (hanzo-kernel quant.rs, "dp4a matvec", "PACKED dp4a matvec"):
+ *   out[n] = sum_b d[n,b] * xd[b] * sum_{j<32} q[n,b,j] * xq[32b + j]
+ * the inner sum an exact integer dot product (dp4a). blocks as in
+ * gai4_q8_0_gemv; xq [K] int8 and xd [K/32] float32 as written by
+ * gai4_quantize_x_q8; out [N] float32. K a multiple of 32; blocks and xq
+ * 16-byte aligned, xd 4-byte aligned.
+ */
+gai4_status gai4_q8_0_gemv_i8(const uint32_t* blocks, const int8_t* xq, const float* xd, float* out,
+                              int64_t N, int64_t K, void* stream);
+
+/*
  * gai4_q4_k_gemv -- Q4_K super-block matrix-vector product
  * (hanzo-kernel quant.rs, Q4_K section, matvec_q4k):
  *   blocks [N, K/256, 144] bytes: d (f16, bytes 0-1, little-endian), dmin

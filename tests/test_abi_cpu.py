@@ -130,3 +130,13 @@ def test_batched_workspace_bytes(lib):
     gather = (3 * 33 * 14336 * 2 + 255) // 256 * 256
     assert got == gather + g4.gai4_qmm_t_workspace_bytes(33, 4096, 14336, 4, 64, torch.bfloat16, 0)
     assert g4.gai4_qmm_t_batched_workspace_bytes(0, 33, 4096, 14336, 4, 64, torch.bfloat16, 0) == 0
+
+
+def test_int8_activation_entry_points_reject_bad_arguments(lib):
+    A = _fake()
+    assert lib.gai4_quantize_x_q8(A, A, A, 48, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_quantize_x_q8(None, A, A, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_quantize_x_q8(A, _fake(0x10008), A, 64, None) == g4.GAI4_ERR_MISALIGNED
+    assert lib.gai4_q8_0_gemv_i8(A, A, A, A, 4, 40, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q8_0_gemv_i8(A, A, _fake(0x10002), A, 4, 64, None) == g4.GAI4_ERR_MISALIGNED
+    assert lib.gai4_q8_0_gemv_i8(A, _fake(0x10004), A, A, 4, 64, None) == g4.GAI4_ERR_MISALIGNED
