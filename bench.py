@@ -212,6 +212,30 @@ def build_batched(torch, g4, dev, seed=7):
     return out
 
 
+# large-M (prefill) qmm_t, measured beside the step (not part of it): (K, N, M);
+# 4096x4096 at M=512 is tensor-bound (about 400 flop per byte), 14336x4096 at
+# M=2048 more so
+PREFILL_SHAPES = [(4096, 4096, 512), (4096, 14336, 2048)]
+
+
+def build_prefill(torch, g4, dev, seed=11):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    bf = torch.bfloat16
+    out = []
+    for (K, N, M) in PREFILL_SHAPES:
+        w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * 0.02
+        p, s, b = g4.gai4_quantize(w, BITS, GS, bf)
+        del w
+        x = torch.randn((M, K), generator=gen, device=dev).to(bf)
+        ws = g4.gai4_qmm_t_workspace_bytes(M, N, K, BITS, GS, bf, 0)
+        wsp = torch.empty(max(ws, 16) // 4 + 4, dtype=torch.float32, device=dev)
+        out.append(dict(kind="qmm_t", p=p, s=s, b=b, x=x, out=torch.empty((M, N), dtype=bf, device=dev), ws=wsp,
+                        M=M, N=N, K=K, bytes=affine_bytes(M, N, K)))
+    torch.cuda.synchronize()
+    return out
+
+
 def q8_i8_bytes(N, K):
     return N * (K // 32) * 36 + K + (K // 32) * 4 + N * 4
 
@@ -420,12 +444,15 @@ def run_gpu(args, rank, world, local_rank):
 
     per_call = None if args.no_per_call else time_per_call(torch, g4, calls, stream, fams)
     # batched / strided qmm_t beside the step (same cold-L2 per-call timing)
-    extra = extra_i8 = None
+    extra = extra_i8 = extra_pf = None
     if not args.no_per_call and not args.only:
         bcalls = build_batched(torch, g4, dev)
         extra = time_per_call(torch, g4, {"qmm_t_batched": bcalls}, stream, ["qmm_t_batched"])
         icalls = build_q8_i8(torch, g4, dev)
         extra_i8 = time_per_call(torch, g4, {"q8_0_i8": icalls}, stream, ["q8_0_i8"])
+        pcalls = build_prefill(torch, g4, dev)
+        extra_pf = time_per_call(torch, g4, {"prefill": pcalls}, stream, ["prefill"])
+        del pcalls
 
     # end to end through the public API: per step, H2D of every call's
     # activations from pinned host memory, the calls, D2H of every output
@@ -473,6 +500,7 @@ def run_gpu(args, rank, world, local_rank):
         "per_call_cold_l2": per_call,
         "batched_cold_l2": extra,
         "q8_0_int8_activations_cold_l2": extra_i8,
+        "prefill_qmm_t_cold_l2": extra_pf,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,
@@ -535,9 +563,10 @@ def time_per_call(torch, g4, calls, stream, fams, reps=8):
                 # min(HBM, tensor) roofline: the call cannot beat the larger of
                 # its byte time and its bf16 tensor-core time
                 flops = 2.0 * c.get("B", 1) * c["M"] * c["N"] * c["K"]
-                roof_us = max(c["bytes"] / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+                hbm_us, tc_us = c["bytes"] / (hbm * 1e9) * 1e6, flops / (tflops * 1e12) * 1e6
                 rec.update({"TFLOP/s": round(flops / (us * 1e-6) / 1e12, 2),
-                            "frac_of_roofline": round(roof_us / us, 3)})
+                            "bound": "tensor" if tc_us > hbm_us else "hbm",
+                            "frac_of_roofline": round(max(hbm_us, tc_us) / us, 3)})
             out.append(rec)
     del flush
     return out

@@ -54,6 +54,7 @@ SIGNATURES = {
     "gai4_quantize_x_q8": ([_P, _P, _P, _I64, _P], _I),
     "gai4_q8_0_gemv_i8": ([_P, _P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
+    "gai4_check_bounded_wait": ([_I, _I64, _P, _P], _I),
 }
 
 
@@ -294,3 +295,16 @@ def gai4_q4_k_gemv(blocks, x, out=None, stream=None):
 def gai4_last_device_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device status word."""
     return int(lib().gai4_last_device_status(_stream(stream)))
+
+
+def gai4_check_bounded_wait(arrive: bool, limit_cycles: int, status: torch.Tensor | None = None, stream=None) -> int:
+    """Run the library's bounded mbarrier wait on a barrier that completes
+    (arrive=True) or that nothing completes (arrive=False); returns the value
+    of the device status word `status` (int32 [1], zeroed here when not given)
+    after the stream has finished: 0, or GAI4_ERR_TIMEOUT when the wait gave up."""
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=torch.cuda.current_device())
+    _check("gai4_check_bounded_wait", lib().gai4_check_bounded_wait(1 if arrive else 0, int(limit_cycles),
+                                                                   _ptr(status), _stream(stream)))
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+    return int(status.item())

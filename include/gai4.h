@@ -266,6 +266,23 @@ gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out,
  */
 gai4_status gai4_last_device_status(void* stream);
 
+/*
+ * gai4_check_bounded_wait -- diagnostic of the in-kernel time-out path (no
+ * counterpart on the pages). Every kernel that waits on an mbarrier bounds
+ * the wait: after a limit of SM clock cycles it stops waiting, tells the
+ * CTA's other roles to stop, records GAI4_ERR_TIMEOUT and returns, so that a
+ * lost copy ends the kernel with a status instead of hanging the GPU. This
+ * call launches one warp that runs that same wait, with `limit_cycles`
+ * (1 .. 4e9), on a shared-memory barrier that one of its threads completes
+ * (arrive != 0: the wait succeeds and *status is left as it was) or that
+ * nothing completes (arrive == 0: the wait gives up after about limit_cycles
+ * cycles and sets *status = GAI4_ERR_TIMEOUT).
+ *   status: device int, 4-byte aligned, written by the kernel (caller-owned;
+ *   the library's own status word is not touched).
+ * Asynchronous on `stream`; the context stays usable either way.
+ */
+gai4_status gai4_check_bounded_wait(int arrive, int64_t limit_cycles, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -140,3 +140,11 @@ def test_int8_activation_entry_points_reject_bad_arguments(lib):
     assert lib.gai4_q8_0_gemv_i8(A, A, A, A, 4, 40, None) == g4.GAI4_ERR_INVALID_ARG
     assert lib.gai4_q8_0_gemv_i8(A, A, _fake(0x10002), A, 4, 64, None) == g4.GAI4_ERR_MISALIGNED
     assert lib.gai4_q8_0_gemv_i8(A, _fake(0x10004), A, A, 4, 64, None) == g4.GAI4_ERR_MISALIGNED
+
+
+def test_bounded_wait_check_rejects_bad_arguments(lib):
+    A = _fake()
+    assert lib.gai4_check_bounded_wait(0, 1000, None, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_check_bounded_wait(0, 0, A, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_check_bounded_wait(0, 4000000001, A, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_check_bounded_wait(1, 1000, _fake(0x10002), None) == g4.GAI4_ERR_MISALIGNED
