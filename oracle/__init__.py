@@ -1,4 +1,5 @@
-"""CPU oracle for the affine group-quantized GEMV/GEMM and the Q8_0 / Q4_K GEMVs.
+"""CPU oracle for the affine group-quantized GEMV/GEMM and the Q8_0 / Q4_K
+(and 34-byte Q8_0 / Q6_K) GEMVs.
 
 TEST INFRASTRUCTURE ONLY. Only the test suite, ``__graft_entry__.smoke()`` and
 the CPU-baseline leg of ``bench.py`` may import this package. It shares no code
@@ -67,9 +68,15 @@ def lib():
         L.orc_q8_0_block_dot_i8.argtypes = [P, P]
         L.orc_q8_0_block_dot_i8.restype = ctypes.c_int64
         L.orc_q8_0_gemv_i8.argtypes = [P, P, P, I64, I64, P, I64, P, P]
+        L.orc_q8_0_34b_dequant_block.argtypes = [P, P]
+        L.orc_q8_0_34b_gemv.argtypes = [P, P, I64, I64, P, I64, P, P]
+        L.orc_q6_k_code.argtypes = [P, I]
+        L.orc_q6_k_dequant_block.argtypes = [P, P]
+        L.orc_q6_k_gemv.argtypes = [P, P, I64, I64, P, I64, P, P]
         for name in ("orc_unpack", "orc_pack", "orc_quantize", "orc_dequantize", "orc_qmm",
                      "orc_q8_0_dequant_block", "orc_q8_0_gemv", "orc_q4_k_dequant_block",
-                     "orc_q4_k_gemv"):
+                     "orc_q4_k_gemv", "orc_q8_0_34b_dequant_block", "orc_q8_0_34b_gemv", "orc_q6_k_code",
+                     "orc_q6_k_dequant_block", "orc_q6_k_gemv"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -275,4 +282,53 @@ def q4_k_gemv(blocks: np.ndarray, x: np.ndarray, rows=None):
     absdot = np.zeros(nr, dtype=np.float64)
     _check(lib().orc_q4_k_gemv(_p(blocks), _p(x), N, K, _p(r), nr, _p(out), _p(absdot)),
            "q4_k_gemv")
+    return out, absdot
+
+
+def q8_0_34b_dequant_block(block34: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(block34, dtype=np.uint8).reshape(34)
+    out = np.zeros(32, dtype=np.float64)
+    _check(lib().orc_q8_0_34b_dequant_block(_p(b), _p(out)), "q8_0_34b_dequant_block")
+    return out
+
+
+def q8_0_34b_gemv(blocks: np.ndarray, x: np.ndarray, rows=None):
+    """blocks u8 [N, K/32, 34] (GGUF's own Q8_0 block), x f32 [K] -> (out f64, absdot f64)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    N = blocks.shape[0]
+    K = x.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros(nr, dtype=np.float64)
+    absdot = np.zeros(nr, dtype=np.float64)
+    _check(lib().orc_q8_0_34b_gemv(_p(blocks), _p(x), N, K, _p(r), nr, _p(out), _p(absdot)),
+           "q8_0_34b_gemv")
+    return out, absdot
+
+
+def q6_k_codes(block210: np.ndarray) -> np.ndarray:
+    """The 256 signed 6-bit codes (-32..31) of one Q6_K super-block."""
+    b = np.ascontiguousarray(block210, dtype=np.uint8).reshape(210)
+    return np.array([lib().orc_q6_k_code(_p(b), e) for e in range(256)], dtype=np.int64)
+
+
+def q6_k_dequant_block(block210: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(block210, dtype=np.uint8).reshape(210)
+    out = np.zeros(256, dtype=np.float64)
+    _check(lib().orc_q6_k_dequant_block(_p(b), _p(out)), "q6_k_dequant_block")
+    return out
+
+
+def q6_k_gemv(blocks: np.ndarray, x: np.ndarray, rows=None):
+    """blocks u8 [N, K/256, 210], x f32 [K] -> (out f64, absdot f64)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    N = blocks.shape[0]
+    K = x.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros(nr, dtype=np.float64)
+    absdot = np.zeros(nr, dtype=np.float64)
+    _check(lib().orc_q6_k_gemv(_p(blocks), _p(x), N, K, _p(r), nr, _p(out), _p(absdot)), "q6_k_gemv")
     return out, absdot

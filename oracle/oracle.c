@@ -31,6 +31,9 @@
  *  - hanzo-kernel quant.rs: Q8_0 (one f16 scale + 32 int8 per block; packed
  *    9-word block, scale in the low half of word 0), Q4_K (144-byte super-block
  *    d, dmin, scales[12], qs[128]; get_scale_min_k4; w = d*sc*q - dmin*m).
+ *  - hanzo-kernel quant.rs names Q6_K and the 34-byte Q8_0 block without
+ *    writing them out; their layouts are read from the GGUF format's
+ *    published block definitions (section "GGUF block layouts" below).
  *
  * Where the pages leave a step open, the reading taken is stated at the
  * function that takes it.
@@ -493,6 +496,113 @@ int orc_q4_k_gemv(const uint8_t* blocks, const float* x, int64_t N, int64_t K,
         double acc = 0.0, aacc = 0.0;
         for (int64_t b = 0; b < nb; ++b) {
             orc_q4_k_dequant_block(blocks + (n * nb + b) * 144, w256);
+            for (int i = 0; i < 256; ++i) {
+                double p = w256[i] * (double)x[b * 256 + i];
+                acc += p;
+                aacc += fabs(p);
+            }
+        }
+        out[j] = acc;
+        if (absdot) absdot[j] = aacc;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GGUF block layouts beyond the pages: the 34-byte Q8_0 block and Q6_K      */
+/* ------------------------------------------------------------------------ */
+/*
+ * hanzo-kernel quant.rs names Q6_K beside Q4_K as following the same shape
+ * (a block decode feeding the same contraction) and describes its Q8_0
+ * "production layout" as the 34-byte block re-packed into nine 32-bit words.
+ * Neither block layout is written out on the pages. Reading taken here: the
+ * GGUF file format's published block definitions.
+ *  - Q8_0, 34 bytes per 32 weights: bytes 0..1 the scale d (f16,
+ *    little-endian), bytes 2..33 the codes q_0..q_31 (int8); w_j = d * q_j.
+ *    The same (d, q) as the nine-word block, without the padding.
+ *  - Q6_K, 210 bytes per 256 weights: ql[128] (bytes 0..127) the low four
+ *    bits of the codes, qh[64] (bytes 128..191) the high two bits, sc[16]
+ *    (bytes 192..207) signed 8-bit scales, one per 16 weights, d (bytes
+ *    208..209, f16). Element e = 128h + 32c + l (h < 2, c < 4, l < 32):
+ *      low  = nibble c/2 (low nibble first) of ql[64h + 32(c%2) + l]
+ *      high = bits 2c..2c+1 of qh[32h + l]
+ *      q_e  = (low + 16*high) - 32            (in -32..31)
+ *      w_e  = d * sc[e/16] * q_e
+ *    (e/16 = 8h + 2c + l/16: each 16 consecutive weights share a scale.)
+ */
+
+/* 34-byte Q8_0 block -> 32 weights */
+int orc_q8_0_34b_dequant_block(const uint8_t* blk, double* w32)
+{
+    double d = orc_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+    for (int j = 0; j < 32; ++j) {
+        int q = blk[2 + j] >= 128 ? (int)blk[2 + j] - 256 : (int)blk[2 + j];
+        w32[j] = d * (double)q;
+    }
+    return ORC_OK;
+}
+
+/* out[j] = sum_k w[rows[j], k] * x[k]; blocks [N][K/32][34] bytes (binary64) */
+int orc_q8_0_34b_gemv(const uint8_t* blocks, const float* x, int64_t N, int64_t K,
+                      const int64_t* rows, int64_t nrows, double* out, double* absdot)
+{
+    if (N < 0 || K <= 0 || K % 32) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t nb = K / 32;
+    double w32[32];
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) return ORC_EINVAL;
+        double acc = 0.0, aacc = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            orc_q8_0_34b_dequant_block(blocks + (n * nb + b) * 34, w32);
+            for (int i = 0; i < 32; ++i) {
+                double p = w32[i] * (double)x[b * 32 + i];
+                acc += p;
+                aacc += fabs(p);
+            }
+        }
+        out[j] = acc;
+        if (absdot) absdot[j] = aacc;
+    }
+    return ORC_OK;
+}
+
+/* the signed 6-bit code q_e (-32..31) of element e of a Q6_K super-block */
+int orc_q6_k_code(const uint8_t* blk, int e)
+{
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    int h = e / 128, c = (e / 32) % 4, l = e % 32;
+    int low = (ql[64 * h + 32 * (c % 2) + l] >> (4 * (c / 2))) & 15;
+    int high = (qh[32 * h + l] >> (2 * c)) & 3;
+    return low + 16 * high - 32;
+}
+
+/* 210-byte Q6_K super-block -> 256 weights */
+int orc_q6_k_dequant_block(const uint8_t* blk, double* w256)
+{
+    const int8_t* sc = (const int8_t*)(blk + 192);
+    double d = orc_f16_to_f64((uint16_t)(blk[208] | (blk[209] << 8)));
+    for (int e = 0; e < 256; ++e)
+        w256[e] = d * (double)sc[e / 16] * (double)orc_q6_k_code(blk, e);
+    return ORC_OK;
+}
+
+/* out[j] = sum_k w[rows[j], k] * x[k]; blocks [N][K/256][210] bytes (binary64) */
+int orc_q6_k_gemv(const uint8_t* blocks, const float* x, int64_t N, int64_t K,
+                  const int64_t* rows, int64_t nrows, double* out, double* absdot)
+{
+    if (N < 0 || K <= 0 || K % 256) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t nb = K / 256;
+    double w256[256];
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) return ORC_EINVAL;
+        double acc = 0.0, aacc = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            orc_q6_k_dequant_block(blocks + (n * nb + b) * 210, w256);
             for (int i = 0; i < 256; ++i) {
                 double p = w256[i] * (double)x[b * 256 + i];
                 acc += p;

@@ -13,6 +13,11 @@ Distributions follow the workloads the pages describe:
     stored as f16 in the low half of word 0 (high half zero), 9 words/block;
   * Q4_K super-blocks: d, dmin ~ U(1e-4, 1e-2) stored as f16, 12 scale bytes
     and 128 qs bytes uniform random, 144 bytes/block.
+  * GGUF's own 34-byte Q8_0 blocks: the Q8_0 distributions above, f16 scale in
+    bytes 0..1, the 32 codes in bytes 2..33.
+  * Q6_K super-blocks: 128 ql and 64 qh bytes uniform random, 16 int8 scales
+    uniform in [-128, 127], d ~ U(1e-4, 1e-2) stored as f16 in bytes 208..209,
+    210 bytes/block.
 
 f16/bf16 arrays are returned as numpy uint16 bit patterns.
 """
@@ -69,6 +74,30 @@ def q4_k_blocks(N: int, K: int, seed: int) -> np.ndarray:
     dmin = r.uniform(1e-4, 1e-2, size=(N, nb)).astype(np.float32).astype(np.float16)
     blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, nb, 2)
     blocks[:, :, 2:4] = dmin.view(np.uint8).reshape(N, nb, 2)
+    return blocks
+
+
+def q8_0_34b_blocks(N: int, K: int, seed: int) -> np.ndarray:
+    """uint8 [N, K/32, 34] GGUF Q8_0 blocks (f16 scale, then 32 int8 codes)."""
+    assert K % 32 == 0
+    r = rng(seed)
+    nb = K // 32
+    d = r.uniform(1e-4, 1e-2, size=(N, nb)).astype(np.float32).astype(np.float16)
+    q = r.integers(-127, 128, size=(N, nb, 32), dtype=np.int64).astype(np.int8)
+    blocks = np.empty((N, nb, 34), dtype=np.uint8)
+    blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:] = q.view(np.uint8)
+    return blocks
+
+
+def q6_k_blocks(N: int, K: int, seed: int) -> np.ndarray:
+    """uint8 [N, K/256, 210] Q6_K super-blocks."""
+    assert K % 256 == 0
+    r = rng(seed)
+    nb = K // 256
+    blocks = r.integers(0, 256, size=(N, nb, 210), dtype=np.int64).astype(np.uint8)
+    d = r.uniform(1e-4, 1e-2, size=(N, nb)).astype(np.float32).astype(np.float16)
+    blocks[:, :, 208:210] = d.view(np.uint8).reshape(N, nb, 2)
     return blocks
 
 

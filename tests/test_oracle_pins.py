@@ -454,3 +454,136 @@ def test_q8_0_gemv_i8_closed_form():
     got, _ = oracle.q8_0_gemv_i8(blocks, xq, xd)
     dw = (blocks[:, :, 0] & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
     np.testing.assert_array_equal(got, 32 * (dw * xd.astype(np.float64)).sum(axis=1))
+
+
+# --------------------------------------------------------------------------
+# GGUF block layouts beyond the pages (34-byte Q8_0, Q6_K). The layouts are a
+# reading (the GGUF format's published block definitions); these pins tie the
+# oracle to that reading through a second, byte-oriented formulation.
+# --------------------------------------------------------------------------
+
+def _q8_0_34b_from_words(blocks9):
+    """the same (d, q) as a nine-word Q8_0 block, in the 34-byte layout"""
+    N, nb, _ = blocks9.shape
+    out = np.empty((N, nb, 34), dtype=np.uint8)
+    out[:, :, 0:2] = (blocks9[:, :, 0] & 0xFFFF).astype(np.uint16).view(np.uint8).reshape(N, nb, 2)
+    out[:, :, 2:] = np.ascontiguousarray(blocks9[:, :, 1:]).view(np.uint8).reshape(N, nb, 32)
+    return out
+
+
+def test_q8_0_34b_equals_nine_word_layout():
+    N, K = 7, 320
+    b9 = synth.q8_0_blocks(N, K, 71)
+    b34 = _q8_0_34b_from_words(b9)
+    x = synth.f32_vector(K, 72)
+    want, wabs = oracle.q8_0_gemv(b9, x)
+    got, gabs = oracle.q8_0_34b_gemv(b34, x)
+    assert np.array_equal(got, want) and np.array_equal(gabs, wabs)
+
+
+def test_q8_0_34b_block_decode_by_numpy():
+    b = synth.q8_0_34b_blocks(3, 64, 73)
+    for blk in b.reshape(-1, 34):
+        d = float(blk[0:2].copy().view(np.float16)[0])
+        q = blk[2:].view(np.int8).astype(np.float64)
+        assert np.array_equal(oracle.q8_0_34b_dequant_block(blk), d * q)
+
+
+def _q6_k_encode(u, sc, d_f16):
+    """Q6_K super-block from unsigned codes u = q + 32 (0..63), 16 int8 scales
+    and an f16 d, built byte by byte: ql byte i of half h (i = 64h + r) holds
+    element 128h + r in its low nibble and element 128h + 64 + r in its high
+    nibble; qh byte 32h + l holds the top two bits of elements 128h + l,
+    128h + 32 + l, 128h + 64 + l, 128h + 96 + l at bits 0-1, 2-3, 4-5, 6-7."""
+    u = [int(v) for v in u]
+    blk = bytearray(210)
+    for i in range(128):
+        h, r = divmod(i, 64)
+        blk[i] = (u[128 * h + r] & 15) | ((u[128 * h + 64 + r] & 15) << 4)
+    for i in range(64):
+        h, l = divmod(i, 32)
+        v = 0
+        for k in range(4):
+            v |= ((u[128 * h + 32 * k + l] >> 4) & 3) << (2 * k)
+        blk[128 + i] = v
+    blk[192:208] = np.asarray(sc, dtype=np.int8).tobytes()
+    blk[208:210] = np.asarray([d_f16], dtype=np.float16).tobytes()
+    return np.frombuffer(bytes(blk), dtype=np.uint8).copy()
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_q6_k_round_trip_through_encoder(seed):
+    r = np.random.default_rng(seed)
+    q = r.integers(-32, 32, size=256)
+    sc = r.integers(-128, 128, size=16)
+    d = np.float16(r.uniform(1e-3, 1e-1))
+    blk = _q6_k_encode(q + 32, sc, d)
+    assert np.array_equal(oracle.q6_k_codes(blk), q)
+    want = float(d) * sc[np.arange(256) // 16].astype(np.float64) * q.astype(np.float64)
+    assert np.array_equal(oracle.q6_k_dequant_block(blk), want)
+
+
+def test_q6_k_every_code_value_and_range():
+    blk = _q6_k_encode(np.arange(256) % 64, np.ones(16, dtype=np.int64), np.float16(1.0))
+    codes = oracle.q6_k_codes(blk)
+    assert np.array_equal(codes, np.arange(256) % 64 - 32)
+    rnd = synth.q6_k_blocks(4, 1024, 74).reshape(-1, 210)
+    allc = np.concatenate([oracle.q6_k_codes(b) for b in rnd])
+    assert allc.min() == -32 and allc.max() == 31 and len(np.unique(allc)) == 64
+
+
+def test_q6_k_zero_bytes_closed_form():
+    """ql = qh = 0: every code is -32, so w_e = -32 * d * sc[e // 16]."""
+    sc = np.arange(-8, 8, dtype=np.int64) * 9
+    blk = _q6_k_encode(np.zeros(256, dtype=np.int64), sc, np.float16(0.5))
+    assert np.array_equal(oracle.q6_k_dequant_block(blk), -16.0 * sc[np.arange(256) // 16].astype(np.float64))
+
+
+def test_q6_k_single_bit_moves_one_code():
+    """Each of the 1536 code bits (ql, qh) changes exactly one element's code, by
+    the bit's weight (1, 2, 4, 8 for ql nibble bits, 16 or 32 for qh bits), and
+    all 256 elements x 6 bits are reached exactly once."""
+    base = np.zeros(210, dtype=np.uint8)
+    base[192:208] = 1
+    base[208:210] = np.frombuffer(np.float16(1.0).tobytes(), dtype=np.uint8)
+    q0 = oracle.q6_k_codes(base)
+    seen = {}
+    for byte in range(192):
+        for bit in range(8):
+            blk = base.copy()
+            blk[byte] = 1 << bit
+            diff = oracle.q6_k_codes(blk) - q0
+            nz = np.flatnonzero(diff)
+            assert len(nz) == 1, (byte, bit)
+            e = int(nz[0])
+            step = int(diff[e])
+            if byte < 128:
+                assert step == 1 << (bit % 4)
+            else:
+                assert step == 16 << (bit % 2)
+            key = (e, step)
+            assert key not in seen
+            seen[key] = (byte, bit)
+    assert len(seen) == 256 * 6
+
+
+def test_q6_k_gemv_exact_rational():
+    from fractions import Fraction
+    r = np.random.default_rng(5)
+    N, K = 3, 512
+    q = r.integers(-32, 32, size=(N, K // 256, 256))
+    sc = r.integers(-128, 128, size=(N, K // 256, 16))
+    d = r.uniform(1e-3, 1e-1, size=(N, K // 256)).astype(np.float16)
+    blocks = np.stack([np.stack([_q6_k_encode(q[n, b] + 32, sc[n, b], d[n, b]) for b in range(K // 256)])
+                       for n in range(N)])
+    x = synth.f32_vector(K, 75)
+    got, _ = oracle.q6_k_gemv(blocks, x)
+    for n in range(N):
+        exact, mag = Fraction(0), Fraction(0)
+        for k in range(K):
+            b, e = divmod(k, 256)
+            t = Fraction(float(d[n, b])) * int(sc[n, b, e // 16]) * int(q[n, b, e]) * Fraction(float(x[k]))
+            exact += t
+            mag += abs(t)
+        # K binary64 additions: |error| <= K * 2^-53 * sum |terms|
+        assert abs(Fraction(got[n]) - exact) <= mag * K / Fraction(2 ** 53)
