@@ -253,6 +253,26 @@ def build_q8_i8(torch, g4, dev):
     return out
 
 
+def gguf_bytes(kind, N, K):
+    blk = N * (K // 32) * 34 if kind == "q8_0_34b" else N * (K // 256) * 210
+    return blk + 4 * K + 4 * N
+
+
+def build_gguf(torch, g4, dev):
+    """GGUF's 34-byte Q8_0 blocks and Q6_K super-blocks (f32 activations),
+    measured beside the step at the Q8_0 / Q4_K shapes."""
+    import synth
+    out = []
+    for i, (N, K) in enumerate(BLOCKQ_SHAPES):
+        x = torch.from_numpy(synth.f32_vector(K, 311 + i)).to(dev)
+        for kind, gen in (("q8_0_34b", synth.q8_0_34b_blocks), ("q6_k", synth.q6_k_blocks)):
+            blk = torch.from_numpy(gen(N, K, 312 + i)).to(dev)
+            out.append(dict(kind=kind, blocks=blk, x=x, out=torch.empty(N, device=dev), N=N, K=K,
+                            bytes=gguf_bytes(kind, N, K)))
+    torch.cuda.synchronize()
+    return out
+
+
 def build_workload(torch, g4, dev, seed=0, only=None):
     """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
@@ -316,6 +336,10 @@ def issue(g4, c):
         g4.gai4_q8_0_gemv_i8(c["blocks"], c["xq"], c["xd"], out=c["out"])
     elif k == "q8_0":
         g4.gai4_q8_0_gemv(c["blocks"], c["x"], out=c["out"])
+    elif k == "q8_0_34b":
+        g4.gai4_q8_0_34b_gemv(c["blocks"], c["x"], out=c["out"])
+    elif k == "q6_k":
+        g4.gai4_q6_k_gemv(c["blocks"], c["x"], out=c["out"])
     else:
         g4.gai4_q4_k_gemv(c["blocks"], c["x"], out=c["out"])
 
@@ -444,12 +468,15 @@ def run_gpu(args, rank, world, local_rank):
 
     per_call = None if args.no_per_call else time_per_call(torch, g4, calls, stream, fams)
     # batched / strided qmm_t beside the step (same cold-L2 per-call timing)
-    extra = extra_i8 = extra_pf = None
+    extra = extra_i8 = extra_pf = extra_gg = None
     if not args.no_per_call and not args.only:
         bcalls = build_batched(torch, g4, dev)
         extra = time_per_call(torch, g4, {"qmm_t_batched": bcalls}, stream, ["qmm_t_batched"])
         icalls = build_q8_i8(torch, g4, dev)
         extra_i8 = time_per_call(torch, g4, {"q8_0_i8": icalls}, stream, ["q8_0_i8"])
+        gcalls = build_gguf(torch, g4, dev)
+        extra_gg = time_per_call(torch, g4, {"gguf": gcalls}, stream, ["gguf"])
+        del gcalls
         pcalls = build_prefill(torch, g4, dev)
         extra_pf = time_per_call(torch, g4, {"prefill": pcalls}, stream, ["prefill"])
         del pcalls
@@ -501,6 +528,7 @@ def run_gpu(args, rank, world, local_rank):
         "batched_cold_l2": extra,
         "q8_0_int8_activations_cold_l2": extra_i8,
         "prefill_qmm_t_cold_l2": extra_pf,
+        "gguf_blocks_cold_l2": extra_gg,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": kernel_launches_per_step(g4, calls, torch) * steps_total,

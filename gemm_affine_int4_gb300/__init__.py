@@ -55,6 +55,8 @@ SIGNATURES = {
     "gai4_q8_0_gemv_i8": ([_P, _P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
     "gai4_check_bounded_wait": ([_I, _I64, _P, _P], _I),
+    "gai4_q8_0_34b_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
+    "gai4_q6_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
 }
 
 
@@ -289,6 +291,27 @@ def gai4_q4_k_gemv(blocks, x, out=None, stream=None):
     if out is None:
         out = torch.empty((N,), dtype=torch.float32, device=x.device)
     _check("gai4_q4_k_gemv", lib().gai4_q4_k_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
+    return out
+
+
+def gai4_q8_0_34b_gemv(blocks, x, out=None, stream=None):
+    """blocks [N, K/32, 34] uint8 (GGUF's 34-byte Q8_0 block), x [K] float32 -> out [N] float32."""
+    N = blocks.shape[0]
+    K = x.shape[-1]
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float32, device=x.device)
+    _check("gai4_q8_0_34b_gemv", lib().gai4_q8_0_34b_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K,
+                                                          _stream(stream)))
+    return out
+
+
+def gai4_q6_k_gemv(blocks, x, out=None, stream=None):
+    """blocks [N, K/256, 210] uint8 (Q6_K super-blocks), x [K] float32 -> out [N] float32."""
+    N = blocks.shape[0]
+    K = x.shape[-1]
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float32, device=x.device)
+    _check("gai4_q6_k_gemv", lib().gai4_q6_k_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
     return out
 
 

@@ -259,6 +259,35 @@ gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out,
                            int64_t N, int64_t K, void* stream);
 
 /*
+ * gai4_q8_0_34b_gemv -- Q8_0 matrix-vector product over GGUF's own 34-byte
+ * block (hanzo-kernel quant.rs describes its nine-word "production layout" as
+ * a re-packing of this block; the byte layout itself is read from the GGUF
+ * format's published block definitions):
+ *   blocks [N, K/32, 34] bytes: bytes 0..1 the f16 scale d (little-endian),
+ *   bytes 2..33 the 32 int8 codes; out[n] = sum_b d[n,b] * sum_j q[n,b,j] x[32b + j].
+ *   x [K] float32, out [N] float32. K a multiple of 32; blocks and x 16-byte
+ *   aligned (rows themselves need not be: a row is K/32 * 34 bytes).
+ */
+gai4_status gai4_q8_0_34b_gemv(const uint8_t* blocks, const float* x, float* out,
+                               int64_t N, int64_t K, void* stream);
+
+/*
+ * gai4_q6_k_gemv -- Q6_K super-block matrix-vector product (hanzo-kernel
+ * quant.rs names Q6_K beside Q4_K; the layout is read from the GGUF format's
+ * published block definitions):
+ *   blocks [N, K/256, 210] bytes: ql[128] (bytes 0..127), qh[64] (128..191),
+ *   sc[16] int8 (192..207), d f16 (208..209). Element e = 128h + 32c + l
+ *   (h < 2, c < 4, l < 32) of a block has the code
+ *     q = (nibble c/2 of ql[64h + 32(c%2) + l], low nibble first)
+ *       + 16 * (bits 2c..2c+1 of qh[32h + l]) - 32          (-32 .. 31)
+ *   and the weight d * sc[e/16] * q. out[n] = sum_k w[n,k] x[k];
+ *   x [K] float32, out [N] float32. K a multiple of 256; blocks and x
+ *   16-byte aligned.
+ */
+gai4_status gai4_q6_k_gemv(const uint8_t* blocks, const float* x, float* out,
+                           int64_t N, int64_t K, void* stream);
+
+/*
  * gai4_last_device_status -- synchronizes `stream`, then reads and clears the
  * current device's status word. Returns GAI4_OK, or GAI4_ERR_TIMEOUT if a
  * bounded wait inside a kernel gave up since the last read (that kernel's

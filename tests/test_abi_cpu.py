@@ -148,3 +148,14 @@ def test_bounded_wait_check_rejects_bad_arguments(lib):
     assert lib.gai4_check_bounded_wait(0, 0, A, None) == g4.GAI4_ERR_INVALID_ARG
     assert lib.gai4_check_bounded_wait(0, 4000000001, A, None) == g4.GAI4_ERR_INVALID_ARG
     assert lib.gai4_check_bounded_wait(1, 1000, _fake(0x10002), None) == g4.GAI4_ERR_MISALIGNED
+
+
+def test_gguf_block_gemvs_reject_bad_arguments(lib):
+    A = _fake()
+    assert lib.gai4_q8_0_34b_gemv(None, A, A, 4, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q8_0_34b_gemv(A, A, A, 4, 48, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q8_0_34b_gemv(A, A, A, 0, 64, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q8_0_34b_gemv(_fake(0x10002), A, A, 4, 64, None) == g4.GAI4_ERR_MISALIGNED
+    assert lib.gai4_q6_k_gemv(A, A, None, 4, 256, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q6_k_gemv(A, A, A, 4, 300, None) == g4.GAI4_ERR_INVALID_ARG
+    assert lib.gai4_q6_k_gemv(A, _fake(0x10004), A, 4, 256, None) == g4.GAI4_ERR_MISALIGNED
