@@ -12,10 +12,12 @@
 // Neither block size is a multiple of four bytes, so a block cannot be read in
 // place with aligned word loads. Each warp owns one output row at a time and
 // walks it in slabs of whole blocks (one contiguous run of the row's bytes).
-// A slab is fetched with 16-byte streaming loads starting at the 16-byte
-// boundary at or below it, into registers one slab ahead of the decode; it is
-// then written to a warp-private shared-memory buffer, from which words at
-// 2-byte-aligned offsets are read as two aligned words and a funnel shift.
+// A slab is copied by 16-byte asynchronous copies (cp.async, L2-only), starting
+// at the 16-byte boundary at or below it, into a warp-private ring of
+// shared-memory stages kStages - 1 slabs ahead of the decode (the copy that
+// reaches past the end of the weights reads only the bytes before it and
+// zero-fills the rest); words at 2-byte-aligned offsets are then read from the
+// stage as two aligned words and a funnel shift.
 // A code c becomes a float through the mantissa of 2^23: a byte permute puts
 // c under the exponent byte 0x4B, and one subtraction removes 2^23 and the
 // code's offset (128 for Q8_0 bytes with the sign bit flipped, 32 for Q6_K)
@@ -34,19 +36,22 @@ constexpr int kWarps = 8;   // warps per CTA
 
 template <int FMT>
 struct GgufFmt;
+// kBB bytes per block of kBK weights, kSB blocks per slab, stages of
+// kCPL x 32 16-byte chunks, kStages stages per warp (8 warps x kStages stages
+// fit the 48 KB of static shared memory)
 template <>
 struct GgufFmt<0> {   // Q8_0, 34-byte blocks
-    static constexpr int kBB = 34, kBK = 32, kSB = 32, kCPL = 3;
+    static constexpr int kBB = 34, kBK = 32, kSB = 32, kCPL = 3, kStages = 4;
 };
 template <>
 struct GgufFmt<1> {   // Q6_K, 210-byte super-blocks
-    static constexpr int kBB = 210, kBK = 256, kSB = 8, kCPL = 4;
+    static constexpr int kBB = 210, kBK = 256, kSB = 8, kCPL = 4, kStages = 3;
 };
-// a slab of kSB blocks plus up to 15 leading bytes fits the kCPL x 32 16-byte
-// chunks the lanes hold, and leaves room for the one-word overread of a
-// re-aligned load past the slab's last byte
+// a slab of kSB blocks plus up to 15 leading bytes fits a stage, which leaves
+// room for the one-word overread of a re-aligned load past the slab's last byte
 static_assert(32 * 34 + 15 + 4 <= 3 * 32 * 16, "Q8_0 slab");
 static_assert(8 * 210 + 15 + 4 <= 4 * 32 * 16, "Q6_K slab");
+static_assert(kWarps * 4 * 3 * 512 <= 48 * 1024 && kWarps * 3 * 4 * 512 <= 48 * 1024, "static shared memory");
 
 // the 32-bit word at a 2-byte-aligned shared-memory offset
 __device__ __forceinline__ uint32_t lds_u32_at(const uint8_t* buf, int o) {
@@ -60,12 +65,18 @@ __device__ __forceinline__ float code_f(uint32_t v, float off) {
     return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7650 | k)) - off;
 }
 
-// bytes [g, g + 16) of the buffer, those at or past `total` read as zero
-__device__ __noinline__ uint4 tail_chunk(const uint8_t* p, int64_t g, int64_t total) {
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    for (int b = 0; b < 16; ++b)
-        if (g + b < total) w[b >> 2] |= (uint32_t)p[g + b] << (8 * (b & 3));
-    return make_uint4(w[0], w[1], w[2], w[3]);
+// 16-byte asynchronous copy global -> shared that reads `src_bytes` (1..16)
+// bytes and zero-fills the rest of the 16
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
 // sum over slab `slab` of one Q8_0 row: 8 lanes per block (4 codes each), 4
@@ -137,64 +148,66 @@ __global__ void __launch_bounds__(kWarps * 32) gguf_gemv_kernel(const uint8_t* _
                                                                 const float* __restrict__ x, float* __restrict__ out,
                                                                 int64_t N, int64_t nb, int64_t total) {
     using F = GgufFmt<FMT>;
+    constexpr int kStageBytes = F::kCPL * 512;
     pdl_launch_dependents();
     pdl_wait();   // the kernels before this one are complete: global memory may be read
-    __shared__ __align__(16) uint8_t sbuf[kWarps][F::kCPL * 512];
+    __shared__ __align__(16) uint8_t sbuf[kWarps][F::kStages][kStageBytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t* buf = sbuf[warp];
     const int64_t nslab = (nb + F::kSB - 1) / F::kSB;
     const int64_t wstride = (int64_t)gridDim.x * kWarps;
     const int64_t RB = nb * F::kBB;
+    const int64_t row0 = (int64_t)blockIdx.x * kWarps + warp;
+    // this warp's items: slab t % nslab of row row0 + (t / nslab) * wstride
+    const int64_t n_items = row0 < N ? ((N - 1 - row0) / wstride + 1) * nslab : 0;
 
-    uint4 reg[F::kCPL];
-    int mis = 0;
-    // 16-byte chunks of item (r, s) -- slab s of row r -- into reg; mis = the
-    // slab's offset from the 16-byte boundary below it
-    auto fetch = [&](int64_t r, int64_t s) {
-        const int64_t b0 = s * F::kSB;
-        const int64_t nbs = min((int64_t)F::kSB, nb - b0);
-        const int64_t start = r * RB + b0 * F::kBB;
-        const int64_t a0 = start & ~(int64_t)15;
-        mis = (int)(start - a0);
-        const int nch = (int)((mis + nbs * F::kBB + 15) >> 4);
+    // byte offset of item t's first block in the block array
+    auto item_start = [&](int64_t t) {
+        const int64_t r = row0 + (t / nslab) * wstride, s = t % nslab;
+        return r * RB + s * F::kSB * F::kBB;
+    };
+    auto issue = [&](int64_t t) {
+        if (t < n_items) {
+            const int64_t s = t % nslab;
+            const int64_t nbs = min((int64_t)F::kSB, nb - s * F::kSB);
+            const int64_t start = item_start(t);
+            const int64_t a0 = start & ~(int64_t)15;
+            const int nch = (int)((start - a0 + nbs * F::kBB + 15) >> 4);
+            uint8_t* st = sbuf[warp][t % F::kStages];
 #pragma unroll
-        for (int i = 0; i < F::kCPL; ++i) {
-            const int c = i * 32 + lane;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (c < nch) {
-                const int64_t g = a0 + 16 * (int64_t)c;
-                v = g + 16 <= total ? ld_stream_v4(blocks + g) : tail_chunk(blocks, g, total);
+            for (int i = 0; i < F::kCPL; ++i) {
+                const int c = i * 32 + lane;
+                if (c < nch) {
+                    const int64_t g = a0 + 16 * (int64_t)c;   // g < total: the chunk starts inside the slab
+                    cp_async16(st + 16 * c, blocks + g, (int)min((int64_t)16, total - g));
+                }
             }
-            reg[i] = v;
         }
+        cp_async_commit();   // one group per item (empty past the end) keeps the counting uniform
     };
 
-    int64_t row = (int64_t)blockIdx.x * kWarps + warp;
-    int64_t slab = 0;
-    if (row < N) fetch(row, 0);
-    float acc = 0.f;
-    while (row < N) {
-        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < F::kCPL; ++i) reinterpret_cast<uint4*>(buf)[i * 32 + lane] = reg[i];
-        __syncwarp();
-        const int m = mis;
-        const int64_t cur_row = row, cur_slab = slab;
-        if (++slab == nslab) {
-            slab = 0;
-            row += wstride;
-        }
-        if (row < N) fetch(row, slab);   // in flight during the decode below
+    for (int t = 0; t < F::kStages - 1; ++t) issue(t);
+    float acc = 0.f;
+    for (int64_t t = 0; t < n_items; ++t) {
+        __syncwarp();                  // every lane is done with the stage item t - 1 used
+        issue(t + F::kStages - 1);     // ... which item t + kStages - 1 now refills
+        cp_async_wait<F::kStages - 1>();
+        __syncwarp();                  // item t's chunks from every lane have landed
+        const uint8_t* buf = sbuf[warp][t % F::kStages];
+        const int64_t start = item_start(t);
+        const int m = (int)(start & 15);
+        const int64_t s = t % nslab;
         if constexpr (FMT == 0)
-            acc += decode_q8_0_34(buf, m, x, cur_slab, nb, lane);
+            acc += decode_q8_0_34(buf, m, x, s, nb, lane);
         else
-            acc += decode_q6_k(buf, m, x, cur_slab, nb, lane);
-        if (cur_slab == nslab - 1) {
+            acc += decode_q6_k(buf, m, x, s, nb, lane);
+        if (s == nslab - 1) {
             const float v = warp_sum(acc);
-            if (lane == 0) out[cur_row] = v;
+            if (lane == 0) out[row0 + (t / nslab) * wstride] = v;
             acc = 0.f;
         }
     }
+    cp_async_wait<0>();   // no copy outlives the warp (the trailing groups are empty)
 }
 
 template <int FMT>
@@ -204,7 +217,7 @@ cudaError_t launch_gguf_gemv(const uint8_t* blocks, const float* x, float* out, 
     const int64_t nb = K / F::kBK;
     const int64_t total = N * nb * F::kBB;
     const int64_t want = (N + kWarps - 1) / kWarps;
-    const int64_t cap = 4LL * num_sms();   // 4 CTAs of 8 warps per SM
+    const int64_t cap = 4LL * num_sms();   // 4 CTAs of 8 warps per SM (up to 48 KB of stages each)
     const unsigned grid = (unsigned)(want < cap ? want : cap);
     return launch_pdl(gguf_gemv_kernel<FMT>, dim3(grid), dim3(kWarps * 32), 0, s, blocks, x, out, N, nb, total);
 }
