@@ -99,3 +99,17 @@ def test_tc_full_size_sampled(K, N, M):
     ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16", rows=rows)
     assert_within(got[:, rows], ref, absdot, "bf16", f"qmm_t {K}x{N} M={M}")
     assert np.all(np.isfinite(got))
+
+
+# large M (prefill): the activations span several 256-row chunks along the
+# grid's z dimension, the last one ragged in the first case; the second is the
+# benchmark's prefill shape beside the step
+@pytest.mark.parametrize("N,K,M", [(384, 1024, 1100), (14336, 4096, 2048)])
+def test_tc_large_m_sampled(N, K, M):
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=M)
+    path, _ = g4.gai4_qmm_t_plan(M, N, K, 4, 64, torch.bfloat16)
+    assert path == 1
+    got = to_host_f64(_run(packed, s, b, x, "bf16", split_k=0), "bf16")
+    rows = sample_rows(N, 24, M)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16", rows=rows)
+    assert_within(got[:, rows], ref, absdot, "bf16", f"qmm_t large M {K}x{N} M={M}")
