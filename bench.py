@@ -273,6 +273,55 @@ def build_gguf(torch, g4, dev):
     return out
 
 
+# the other activation dtypes of the qmv shapes, and the bit-width / group-size
+# / M sweep at 4096^2: measured per call beside the step (not part of it)
+SWEEP_QMV_SHAPES = [(5120, 5120), (14336, 5120), (5120, 14336), (27648, 5120)]   # (N, K)
+SWEEP_BITS, SWEEP_GS, SWEEP_M = [2, 3, 4, 6, 8], [32, 64, 128], [1, 8, 64]
+
+
+def affine_bytes_g(M, N, K, bits, gs, tbytes):
+    return N * K * bits // 8 + 2 * N * (K // gs) * tbytes + M * K * tbytes + M * N * tbytes
+
+
+def build_sweep(torch, g4, dev, seed=13):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    calls = []
+
+    def add(M, N, K, bits, gs, T, tag):
+        w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * 0.02
+        p, s, b = g4.gai4_quantize(w, bits, gs, T)
+        del w
+        tb = torch.empty((), dtype=T).element_size()
+        x = torch.randn((K,) if M == 1 else (M, K), generator=gen, device=dev).to(T)
+        c = dict(kind="qmv" if M == 1 else "qmm_t", p=p, s=s, b=b, x=x,
+                 out=torch.empty((N,) if M == 1 else (M, N), dtype=T, device=dev), M=M, N=N, K=K, bits=bits, gs=gs,
+                 dtype=str(T).replace("torch.", ""), tag=tag, bytes=affine_bytes_g(M, N, K, bits, gs, tb))
+        if M > 1:
+            ws = g4.gai4_qmm_t_workspace_bytes(M, N, K, bits, gs, T, 0)
+            c["ws"] = torch.empty(max(ws, 16) // 4 + 4, dtype=torch.float32, device=dev)
+        calls.append(c)
+
+    for T in (torch.float16, torch.float32):
+        for (N, K) in SWEEP_QMV_SHAPES:
+            add(1, N, K, BITS, GS, T, "qmv dtypes")
+    for bits in SWEEP_BITS:
+        for gs in SWEEP_GS:
+            for M in SWEEP_M:
+                add(M, 4096, 4096, bits, gs, torch.bfloat16, "bits x group size x M, 4096^2")
+    torch.cuda.synchronize()
+    return calls
+
+
+def time_sweep(torch, g4, dev, stream):
+    calls = build_sweep(torch, g4, dev)
+    recs = time_per_call(torch, g4, {"sweep": calls}, stream, ["sweep"])
+    for r, c in zip(recs, calls):
+        r.update({"set": c["tag"], "dtype": c["dtype"], "bits": c["bits"], "gs": c["gs"], "M": c["M"]})
+    del calls
+    return recs
+
+
 def build_workload(torch, g4, dev, seed=0, only=None):
     """Seeded synthetic inputs on the device: W ~ N(0, 0.02) quantized on the
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
@@ -325,10 +374,11 @@ def build_workload(torch, g4, dev, seed=0, only=None):
 def issue(g4, c):
     k = c["kind"]
     if k == "qmv":
-        g4.gai4_qmv(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS)
+        g4.gai4_qmv(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=c.get("bits", BITS),
+                    group_size=c.get("gs", GS))
     elif k == "qmm_t":
-        g4.gai4_qmm_t(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
-                      workspace=c["ws"])
+        g4.gai4_qmm_t(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=c.get("bits", BITS),
+                      group_size=c.get("gs", GS), split_k=0, workspace=c["ws"])
     elif k == "qmm_t_batched":
         g4.gai4_qmm_t_batched(c["p"], c["s"], c["b"], c["x"], out=c["out"], bits=BITS, group_size=GS, split_k=0,
                               workspace=c["ws"])
@@ -535,6 +585,12 @@ def run_gpu(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if not args.no_per_call and not args.only:
+        # last, and guarded: a measurement beside the step never costs the step's line
+        try:
+            res["sweep_cold_l2"] = time_sweep(torch, g4, dev, stream)
+        except Exception as e:
+            res["sweep_cold_l2"] = {"error": f"{type(e).__name__}: {e}"[:300]}
     return res
 
 
