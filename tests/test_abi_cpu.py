@@ -159,3 +159,37 @@ def test_gguf_block_gemvs_reject_bad_arguments(lib):
     assert lib.gai4_q6_k_gemv(A, A, None, 4, 256, None) == g4.GAI4_ERR_INVALID_ARG
     assert lib.gai4_q6_k_gemv(A, A, A, 4, 300, None) == g4.GAI4_ERR_INVALID_ARG
     assert lib.gai4_q6_k_gemv(A, _fake(0x10004), A, 4, 256, None) == g4.GAI4_ERR_MISALIGNED
+
+
+def test_planner_properties_sweep(lib):
+    """The split planner over a grid of shapes (host logic through the C ABI):
+    automatic splits stay within 1..4, never split K < 512, fit the workspace
+    they are given and report matching workspace bytes; a forced split S is
+    accepted exactly when K cuts into S equal ranges that are multiples of
+    max(64, group_size) and at least 256 long; the tensor-core path is taken
+    exactly for 16-bit activations, 4-bit codes and M >= 3."""
+    import torch
+    bf = torch.bfloat16
+    for M in (1, 2, 3, 16, 85, 300, 2048):
+        for N in (131, 4096, 14336):
+            for K in (256, 512, 1088, 4096, 17408):
+                for gs in (32, 64, 128):
+                    if K % gs:
+                        continue
+                    path, S = g4.gai4_qmm_t_plan(M, N, K, 4, gs, bf, 0, 1 << 40)
+                    assert path == (1 if M >= 3 else 0)
+                    assert 1 <= S <= 4 and (S == 1 or (K >= 512 and path == 1))
+                    want_ws = S * M * N * 4 if S > 1 else 0
+                    assert g4.gai4_qmm_t_workspace_bytes(M, N, K, 4, gs, bf, 0) == want_ws
+                    # a workspace of one slot less than the automatic plan: fewer pieces
+                    if S > 1:
+                        _, S2 = g4.gai4_qmm_t_plan(M, N, K, 4, gs, bf, 0, (S - 1) * M * N * 4)
+                        assert S2 <= S - 1 or S2 == 1
+                    unit = max(64, gs)
+                    for F in (1, 2, 3, 4):
+                        legal = F == 1 or (K >= 512 and K % (F * unit) == 0 and K // F >= 256)
+                        if legal and (F == 1 or path == 1):
+                            assert g4.gai4_qmm_t_plan(M, N, K, 4, gs, bf, F, 1 << 40) == (path, F)
+                        else:
+                            with pytest.raises(g4.Gai4Error):
+                                g4.gai4_qmm_t_plan(M, N, K, 4, gs, bf, F, 1 << 40)
