@@ -723,7 +723,8 @@ def run_e2e(torch, g4, calls, stream, args):
 
 def _oracle_work(fraction):
     """The oracle on a sample of the step: every call of the step, restricted
-    to a deterministic subset of its output rows (all x rows)."""
+    to a deterministic subset of its output rows (all x rows). Each item is
+    (oracle call, rows, bytes, the plain binary32 loop on the same inputs)."""
     import oracle
     import synth
     items = []
@@ -742,19 +743,27 @@ def _oracle_work(fraction):
             W = synth.affine_weights(nr, K, seed)      # the sampled rows' weights
             packed, s, b = oracle.quantize(W, BITS, GS, "bf16")
             x = synth.activations(M, K, "bf16", seed + 1)
-            byt = affine_bytes(M, N, K) * nr / N
-            prepared.append((lambda rows, p=packed, s_=s, b_=b, x_=x: oracle.qmm(p, s_, b_, x_, BITS, GS, "bf16",
-                                                                              rows=rows), nr, byt))
-        elif kind == "q8_0":
-            blk = synth.q8_0_blocks(nr, K, seed)
-            x = synth.f32_vector(K, seed + 1)
-            prepared.append((lambda rows, b_=blk, x_=x: oracle.q8_0_gemv(b_, x_, rows=rows), nr,
-                             q8_bytes(N, K) * nr / N))
+
+            def f64(rows, p=packed, s_=s, b_=b, x_=x):
+                return oracle.qmm(p, s_, b_, x_, BITS, GS, "bf16", rows=rows)
+
+            def f32(rows, p=packed, s_=s, b_=b, x_=x):
+                return oracle.qmm_f32loop(p, s_, b_, x_, BITS, GS, "bf16", rows=rows)
+            prepared.append((f64, nr, affine_bytes(M, N, K) * nr / N, f32))
         else:
-            blk = synth.q4_k_blocks(nr, K, seed)
+            gen = synth.q8_0_blocks if kind == "q8_0" else synth.q4_k_blocks
+            ref = oracle.q8_0_gemv if kind == "q8_0" else oracle.q4_k_gemv
+            loop = oracle.q8_0_gemv_f32loop if kind == "q8_0" else oracle.q4_k_gemv_f32loop
+            blk = gen(nr, K, seed)
             x = synth.f32_vector(K, seed + 1)
-            prepared.append((lambda rows, b_=blk, x_=x: oracle.q4_k_gemv(b_, x_, rows=rows), nr,
-                             q4k_bytes(N, K) * nr / N))
+
+            def f64(rows, b_=blk, x_=x, f=ref):
+                return f(b_, x_, rows=rows)
+
+            def f32(rows, b_=blk, x_=x, f=loop):
+                return f(b_, x_, rows=rows)
+            byt = (q8_bytes(N, K) if kind == "q8_0" else q4k_bytes(N, K)) * nr / N
+            prepared.append((f64, nr, byt, f32))
     return prepared
 
 
@@ -762,12 +771,13 @@ def _run_work(work, threads):
     """Run every sampled call once: on one thread, or split into row ranges
     over `threads` host threads (the C oracle releases the GIL while it runs)."""
     if threads <= 1:
-        for fn, _, _ in work:
-            fn(None)
+        for w in work:
+            w[0](None)
         return
     from concurrent.futures import ThreadPoolExecutor
     tasks = []
-    for fn, nr, _ in work:
+    for w in work:
+        fn, nr = w[0], w[1]
         chunk = max(1, -(-nr // (4 * threads)))
         for a in range(0, nr, chunk):
             tasks.append((fn, np.arange(a, min(nr, a + chunk), dtype=np.int64)))
@@ -782,7 +792,7 @@ def _timed_sample(target_s, threads, max_frac=1.0):
     frac = 1.0 / 512
     for _ in range(4):   # grow the sample until it takes at least half the target time
         work = _oracle_work(frac)
-        byt = sum(b for _, _, b in work)
+        byt = sum(w[2] for w in work)
         t = time.perf_counter()
         _run_work(work, threads)
         dt = time.perf_counter() - t
@@ -805,10 +815,17 @@ def cpu_baseline(target_s=12.0):
     t = time.perf_counter()
     _run_work(work, threads)
     dt = time.perf_counter() - t
+    # the plain binary32 loops on the same rows (the "reasonable CPU" number)
+    work32 = [(w[3], w[1], w[2]) for w in work]
+    t = time.perf_counter()
+    _run_work(work32, threads)
+    dt32 = time.perf_counter() - t
     return {"value": round(byt / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"every call of the step on {frac:.4%} of its output rows (all x rows), binary64 C oracle, "
                       f"row ranges over {threads} threads, {dt:.1f} s",
-            "single_thread": {"value": round(byt / dt1 / 1e9, 4), "cores": 1, "sample": f"the same rows, {dt1:.1f} s"}}
+            "single_thread": {"value": round(byt / dt1 / 1e9, 4), "cores": 1, "sample": f"the same rows, {dt1:.1f} s"},
+            "fp32_loop": {"value": round(byt / dt32 / 1e9, 4), "cores": threads, "kind": "plain binary32 C loops",
+                          "sample": f"the same rows, row ranges over {threads} threads, {dt32:.1f} s"}}
 
 
 def run_reference(args):
@@ -817,7 +834,7 @@ def run_reference(args):
     threads = host_threads()
     target = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
     _, _, frac, work = _timed_sample(target, threads, max_frac=0.25)
-    byt = sum(b for _, _, b in work)
+    byt = sum(w[2] for w in work)
     steps, byt_total, t_total = [], 0.0, 0.0
     for i in range(args.warmup + args.steps):
         t = time.perf_counter()

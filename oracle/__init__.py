@@ -73,10 +73,14 @@ def lib():
         L.orc_q6_k_code.argtypes = [P, I]
         L.orc_q6_k_dequant_block.argtypes = [P, P]
         L.orc_q6_k_gemv.argtypes = [P, P, I64, I64, P, I64, P, P]
+        L.orc_qmm_f32loop.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, P, I64, P]
+        L.orc_q8_0_gemv_f32loop.argtypes = [P, P, I64, I64, P, I64, P]
+        L.orc_q4_k_gemv_f32loop.argtypes = [P, P, I64, I64, P, I64, P]
         for name in ("orc_unpack", "orc_pack", "orc_quantize", "orc_dequantize", "orc_qmm",
                      "orc_q8_0_dequant_block", "orc_q8_0_gemv", "orc_q4_k_dequant_block",
                      "orc_q4_k_gemv", "orc_q8_0_34b_dequant_block", "orc_q8_0_34b_gemv", "orc_q6_k_code",
-                     "orc_q6_k_dequant_block", "orc_q6_k_gemv"):
+                     "orc_q6_k_dequant_block", "orc_q6_k_gemv", "orc_qmm_f32loop", "orc_q8_0_gemv_f32loop",
+                     "orc_q4_k_gemv_f32loop"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -332,3 +336,45 @@ def q6_k_gemv(blocks: np.ndarray, x: np.ndarray, rows=None):
     absdot = np.zeros(nr, dtype=np.float64)
     _check(lib().orc_q6_k_gemv(_p(blocks), _p(x), N, K, _p(r), nr, _p(out), _p(absdot)), "q6_k_gemv")
     return out, absdot
+
+
+# Plain binary32 loops: a CPU timing baseline (the "reasonable CPU" number
+# timed beside the oracle), not a reference; no test takes them as expected.
+
+def qmm_f32loop(packed, scales, biases, x, bits: int, group_size: int, dtype: str, rows=None):
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales)
+    biases = np.ascontiguousarray(biases)
+    x = np.ascontiguousarray(x)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    M, K = x.shape
+    N = packed.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros((M, nr), dtype=np.float32)
+    _check(lib().orc_qmm_f32loop(_p(packed), _p(scales), _p(biases), _p(x), DTYPES[dtype], bits, group_size, M, N,
+                                 K, _p(r), nr, _p(out)), "qmm_f32loop")
+    return out
+
+
+def q8_0_gemv_f32loop(blocks, x, rows=None):
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint32)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    N, K = blocks.shape[0], x.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros(nr, dtype=np.float32)
+    _check(lib().orc_q8_0_gemv_f32loop(_p(blocks), _p(x), N, K, _p(r), nr, _p(out)), "q8_0_gemv_f32loop")
+    return out
+
+
+def q4_k_gemv_f32loop(blocks, x, rows=None):
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    N, K = blocks.shape[0], x.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = N if r is None else r.shape[0]
+    out = np.zeros(nr, dtype=np.float32)
+    _check(lib().orc_q4_k_gemv_f32loop(_p(blocks), _p(x), N, K, _p(r), nr, _p(out)), "q4_k_gemv_f32loop")
+    return out

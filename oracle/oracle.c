@@ -614,3 +614,97 @@ int orc_q6_k_gemv(const uint8_t* blocks, const float* x, int64_t N, int64_t K,
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Plain binary32 loops: a CPU timing baseline, not a reference              */
+/* ------------------------------------------------------------------------ */
+/*
+ * The same loops as orc_qmm, orc_q8_0_gemv and orc_q4_k_gemv with every
+ * value and the accumulator in binary32: what a plain, untuned CPU
+ * implementation of these products computes. They exist to be timed beside
+ * the binary64 oracle (the "reasonable CPU" number); no test takes them as
+ * the expected result.
+ */
+int orc_qmm_f32loop(const uint32_t* packed, const void* scales, const void* biases, const void* x,
+                    int dtype, int bits, int gs, int64_t M, int64_t N, int64_t K,
+                    const int64_t* rows, int64_t nrows, float* out)
+{
+    if (!valid_affine(bits, gs, N, K) || dtype < 0 || dtype > 2 || M < 0) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t G = K / gs, wpr = K * bits / 32;
+    float* w = (float*)malloc((size_t)K * sizeof(float));
+    float* xv = (float*)malloc((size_t)(M * K + 1) * sizeof(float));
+    if (!w || !xv) { free(w); free(xv); return ORC_EINVAL; }
+    for (int64_t i = 0; i < M * K; ++i) xv[i] = (float)load_t(x, i, dtype);
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) { free(w); free(xv); return ORC_EINVAL; }
+        for (int64_t k = 0; k < K; ++k) {
+            float s = (float)load_t(scales, n * G + k / gs, dtype);
+            float b = (float)load_t(biases, n * G + k / gs, dtype);
+            w[k] = s * (float)get_code(packed + n * wpr, k, bits) + b;
+        }
+        for (int64_t m = 0; m < M; ++m) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc += w[k] * xv[m * K + k];
+            out[m * nrows + j] = acc;
+        }
+    }
+    free(w);
+    free(xv);
+    return ORC_OK;
+}
+
+int orc_q8_0_gemv_f32loop(const uint32_t* blocks, const float* x, int64_t N, int64_t K,
+                          const int64_t* rows, int64_t nrows, float* out)
+{
+    if (N < 0 || K <= 0 || K % 32) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t nb = K / 32;
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) return ORC_EINVAL;
+        float acc = 0.0f;
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint32_t* blk = blocks + (n * nb + b) * 9;
+            float d = (float)orc_f16_to_f64((uint16_t)(blk[0] & 0xffffu));
+            for (int i = 0; i < 32; ++i) {
+                unsigned byte = (blk[1 + i / 4] >> (8 * (i % 4))) & 0xffu;
+                int q = byte >= 128 ? (int)byte - 256 : (int)byte;
+                acc += d * (float)q * x[b * 32 + i];
+            }
+        }
+        out[j] = acc;
+    }
+    return ORC_OK;
+}
+
+int orc_q4_k_gemv_f32loop(const uint8_t* blocks, const float* x, int64_t N, int64_t K,
+                          const int64_t* rows, int64_t nrows, float* out)
+{
+    if (N < 0 || K <= 0 || K % 256) return ORC_EINVAL;
+    if (!rows) nrows = N;
+    const int64_t nb = K / 256;
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        if (n < 0 || n >= N) return ORC_EINVAL;
+        float acc = 0.0f;
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* blk = blocks + (n * nb + b) * 144;
+            float d = (float)orc_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+            float dmin = (float)orc_f16_to_f64((uint16_t)(blk[2] | (blk[3] << 8)));
+            for (int g = 0; g < 4; ++g) {
+                int sc_lo, m_lo, sc_hi, m_hi;
+                orc_q4_k_scale_min(blk + 4, 2 * g, &sc_lo, &m_lo);
+                orc_q4_k_scale_min(blk + 4, 2 * g + 1, &sc_hi, &m_hi);
+                for (int i = 0; i < 32; ++i) {
+                    unsigned qb = blk[16 + 32 * g + i];
+                    acc += (d * (float)sc_lo * (float)(qb & 15u) - dmin * (float)m_lo) * x[b * 256 + 64 * g + i];
+                    acc += (d * (float)sc_hi * (float)(qb >> 4) - dmin * (float)m_hi) * x[b * 256 + 64 * g + 32 + i];
+                }
+            }
+        }
+        out[j] = acc;
+    }
+    return ORC_OK;
+}
