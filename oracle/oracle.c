@@ -15,7 +15,9 @@
  * sequential dot product. The only binary32 arithmetic is in quantize, where
  * the chosen codes depend on it (scale = (max-min)/(2^bits-1), the code
  * rint((w-bias)/scale)), and there it is done in binary32 on purpose so that
- * the codes are the ones a binary32 implementation must produce.
+ * the codes are the ones a binary32 implementation must produce. (The
+ * orc_*_f32loop functions at the end are plain binary32 loops kept only as
+ * a CPU timing baseline; nothing compares against them.)
  *
  * Sources (page title, then the passage):
  *  - metaltile-std quantized.rs, kernel mt_qmv: the qmv sum
