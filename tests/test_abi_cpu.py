@@ -193,3 +193,31 @@ def test_planner_properties_sweep(lib):
                         else:
                             with pytest.raises(g4.Gai4Error):
                                 g4.gai4_qmm_t_plan(M, N, K, 4, gs, bf, F, 1 << 40)
+
+
+def test_plain_c_program_uses_the_library(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links
+    libgai4.so and calls host-only entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_gai4.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "gai4.h"
+int main(void) {
+    int path = -1, splits = -1;
+    gai4_status st = gai4_qmm_t_plan(33, 4096, 14336, 4, 64, GAI4_BF16, 2, (size_t)1 << 30, &path, &splits);
+    gai4_status bad = gai4_qmv(NULL, NULL, NULL, NULL, NULL, GAI4_BF16, 4, 64, 16, 64, NULL);
+    printf("%d %d %d %d %d %s\n", gai4_version(), (int)st, path, splits, (int)bad, gai4_status_string(bad));
+    return 0;
+}
+''')
+    exe = tmp_path / "use_gai4"
+    libdir = os.path.dirname(g4.LIB_PATH)
+    subprocess.check_call([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe), "-L", libdir, "-lgai4", "-Wl,-rpath," + libdir])
+    out = subprocess.check_output([str(exe)], text=True).split()
+    assert out[:5] == [str(g4.gai4_version()), "0", "1", "2", str(g4.GAI4_ERR_INVALID_ARG)]
