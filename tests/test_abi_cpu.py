@@ -221,3 +221,15 @@ int main(void) {
                            "-o", str(exe), "-L", libdir, "-lgai4", "-Wl,-rpath," + libdir])
     out = subprocess.check_output([str(exe)], text=True).split()
     assert out[:5] == [str(g4.gai4_version()), "0", "1", "2", str(g4.GAI4_ERR_INVALID_ARG)]
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without libgai4.so every call raises instead of computing
+    anything on the host."""
+    import torch
+    monkeypatch.setattr(g4, "_lib", None)
+    monkeypatch.setattr(g4, "LIB_PATH", str(tmp_path / "absent" / "libgai4.so"))
+    with pytest.raises(RuntimeError):
+        g4.lib()
+    with pytest.raises(RuntimeError):
+        g4.gai4_qmm_t_plan(8, 128, 256, 4, 64, torch.bfloat16)
