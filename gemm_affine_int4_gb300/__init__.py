@@ -51,6 +51,7 @@ SIGNATURES = {
     "gai4_qmm_t_batched_workspace_bytes": ([_I64, _I64, _I64, _I64, _I, _I, _I, _I], ctypes.c_size_t),
     "gai4_q8_0_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
     "gai4_q4_k_gemv": ([_P, _P, _P, _I64, _I64, _P], _I),
+    "gai4_q4_k_dequantize": ([_P, _P, _I64, _I64, _I, _P], _I),
     "gai4_quantize_x_q8": ([_P, _P, _P, _I64, _P], _I),
     "gai4_q8_0_gemv_i8": ([_P, _P, _P, _P, _I64, _I64, _P], _I),
     "gai4_last_device_status": ([_P], _I),
@@ -291,6 +292,18 @@ def gai4_q4_k_gemv(blocks, x, out=None, stream=None):
     if out is None:
         out = torch.empty((N,), dtype=torch.float32, device=x.device)
     _check("gai4_q4_k_gemv", lib().gai4_q4_k_gemv(_ptr(blocks), _ptr(x), _ptr(out), N, K, _stream(stream)))
+    return out
+
+
+def gai4_q4_k_dequantize(blocks, decoder: int = 0, out=None, stream=None):
+    """blocks [N, K/256, 144] uint8 -> weights [N, K] float32 with the (sc, m)
+    decoder of the TMA-staged GEMV kernel (decoder 0) or the general one (1)."""
+    N = blocks.shape[0]
+    K = blocks.shape[1] * 256
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=blocks.device)
+    _check("gai4_q4_k_dequantize", lib().gai4_q4_k_dequantize(_ptr(blocks), _ptr(out), N, K, decoder,
+                                                              _stream(stream)))
     return out
 
 

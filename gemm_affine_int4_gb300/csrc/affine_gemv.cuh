@@ -65,11 +65,24 @@ __device__ __forceinline__ void load_chunk(const uint32_t* p, uint32_t (&w)[CW])
 
 // ---------------------------------------------------------------------------
 // Decode paths. Each turns a chunk's CW words into NP 32-bit operand registers
-// (decode) and adds sum_e (C + q_e) x_e into an accumulator (dot). kOffset is
-// the C of that path: sum_e q_e x_e = acc - kOffset * sum_e x_e.
-// x fragments: 16-bit activations as E/2 registers (pairs, natural order),
-// binary32 activations as E registers.
+// holding the exact codes q_e (decode: a code is first placed under the
+// exponent of a constant C, giving C + q exactly, and C is then subtracted,
+// also exactly), and adds sum_e q_e x_e into an accumulator (dot). Every
+// product q x is exact before it is summed, so codes that are all zero add
+// exactly zero. x fragments: 16-bit activations as E/2 registers (pairs,
+// natural order), binary32 activations as E registers.
 // ---------------------------------------------------------------------------
+
+// (a - b) on 16-bit pairs of type T (exact here: both operands are C + q and C)
+template <typename T>
+__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (T::kIsBF16)
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 
 // kind 0: 16-bit activations, 2/4-bit codes (and 8-bit codes with f16):
 // one mask extracts codes e and e + 16/BITS (one per 16-bit half).
@@ -79,7 +92,6 @@ struct PathPair16 {
     static constexpr int E = G::E, CW = G::CW;
     static constexpr int EPH = 16 / BITS;          // codes per 16-bit half
     static constexpr int NP = E / 2;
-    static constexpr float kOffset = (float)T::kMagicOffset;
     static constexpr uint32_t kMask = ((1u << BITS) - 1u) * 0x00010001u;
     static constexpr uint32_t kMagic = T::kMagic16 * 0x00010001u;
 
@@ -88,7 +100,7 @@ struct PathPair16 {
         for (int i = 0; i < CW; ++i)
 #pragma unroll
             for (int j = 0; j < EPH; ++j)
-                P[i * EPH + j] = ((w[i] >> (BITS * j)) & kMask) | kMagic;
+                P[i * EPH + j] = sub_pair<T>(((w[i] >> (BITS * j)) & kMask) | kMagic, kMagic);
     }
     __device__ __forceinline__ static float dot(const uint32_t (&P)[NP], const uint32_t* xr, float acc) {
 #pragma unroll
@@ -111,13 +123,12 @@ struct PathPair16 {
 
 // kind 1: bf16 activations, 8-bit codes (bf16 holds 128 + q exactly only for
 // q < 128): split each code into its low and high nibble planes,
-// sum q x = sum lo x + 16 sum hi x; acc = acc_lo + 16 acc_hi, C = 128 * 17.
+// sum q x = sum lo x + 16 sum hi x (both sums of exact products).
 template <typename T>
 struct PathBf16Byte {
     using G = ChunkGeom<8>;
     static constexpr int E = G::E, CW = G::CW;
     static constexpr int NP = E;                   // E/2 low-nibble pairs, E/2 high
-    static constexpr float kOffset = 128.0f * 17.0f;
     static constexpr uint32_t kMask = 0x000F000Fu;
     static constexpr uint32_t kMagic = 0x43004300u;
 
@@ -126,8 +137,8 @@ struct PathBf16Byte {
         for (int i = 0; i < CW; ++i)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                P[i * 2 + j] = ((w[i] >> (8 * j)) & kMask) | kMagic;              // low nibbles
-                P[E / 2 + i * 2 + j] = ((w[i] >> (8 * j + 4)) & kMask) | kMagic;  // high nibbles
+                P[i * 2 + j] = sub_pair<T>(((w[i] >> (8 * j)) & kMask) | kMagic, kMagic);              // low
+                P[E / 2 + i * 2 + j] = sub_pair<T>(((w[i] >> (8 * j + 4)) & kMask) | kMagic, kMagic);  // high
             }
     }
     __device__ __forceinline__ static float dot(const uint32_t (&P)[NP], const uint32_t* xr, float acc) {
@@ -173,12 +184,11 @@ struct PathSingle16 {
     using G = ChunkGeom<BITS>;
     static constexpr int E = G::E, CW = G::CW;
     static constexpr int NP = E;
-    static constexpr float kOffset = (float)T::kMagicOffset;
     static constexpr uint32_t kMask = (1u << BITS) - 1u;
 
     __device__ __forceinline__ static void decode(const uint32_t (&w)[CW], uint32_t (&P)[NP]) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) P[e] = (code_at<BITS, CW>(w, e, 0) & kMask) | T::kMagic16;
+        for (int e = 0; e < E; ++e) P[e] = sub_pair<T>((code_at<BITS, CW>(w, e, 0) & kMask) | T::kMagic16, T::kMagic16);
     }
     __device__ __forceinline__ static float dot(const uint32_t (&P)[NP], const uint32_t* xr, float acc) {
 #pragma unroll
@@ -191,20 +201,22 @@ struct PathSingle16 {
 };
 
 // kind 3: binary32 activations, any width: the code goes into the top BITS
-// mantissa bits of 2^BITS, giving the float 2^BITS + q exactly.
+// mantissa bits of 2^BITS, giving the float 2^BITS + q exactly; subtracting
+// 2^BITS gives q exactly.
 template <int BITS>
 struct PathF32 {
     using G = ChunkGeom<BITS>;
     static constexpr int E = G::E, CW = G::CW;
     static constexpr int NP = E;
-    static constexpr float kOffset = (float)(1 << BITS);
     static constexpr int kDst = 23 - BITS;
     static constexpr uint32_t kMask = ((1u << BITS) - 1u) << kDst;
     static constexpr uint32_t kExp = (uint32_t)(127 + BITS) << 23;
 
     __device__ __forceinline__ static void decode(const uint32_t (&w)[CW], uint32_t (&P)[NP]) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) P[e] = (code_at<BITS, CW>(w, e, kDst) & kMask) | kExp;
+        for (int e = 0; e < E; ++e)
+            P[e] = __float_as_uint(__uint_as_float((code_at<BITS, CW>(w, e, kDst) & kMask) | kExp) -
+                                   (float)(1 << BITS));
     }
     __device__ __forceinline__ static float dot(const uint32_t (&P)[NP], const uint32_t* xr, float acc) {
 #pragma unroll
@@ -367,8 +379,7 @@ __global__ void __launch_bounds__(NW * 32) affine_gemv_kernel(const AffineKernel
                     const float xs = xsum_sm[m * chunks_per_m + c];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float acc = Path::dot(P[r], xr, 0.f);
-                        const float qx = fmaf(-Path::kOffset, xs, acc);      // sum q x of the chunk
+                        const float qx = Path::dot(P[r], xr, 0.f);      // sum q x of the chunk
                         part[r][m] = fmaf(sc[r], qx, fmaf(bc[r], xs, part[r][m]));
                     }
                 }

@@ -273,6 +273,17 @@ gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out, in
     return from_cuda(launch_q4_k_gemv(blocks, x, out, N, K, (cudaStream_t)stream));
 }
 
+gai4_status gai4_q4_k_dequantize(const uint8_t* blocks, float* w_out, int64_t N, int64_t K, int decoder,
+                                 void* stream) {
+    if (!blocks || !w_out || N <= 0 || K <= 0 || K % 256 != 0) return GAI4_ERR_INVALID_ARG;
+    if (decoder != 0 && decoder != 1) return GAI4_ERR_UNSUPPORTED;
+    if (!aligned16(blocks) || ((uintptr_t)w_out & 3u) != 0) return GAI4_ERR_MISALIGNED;
+    const int64_t nblk = N * (K / 256);
+    cudaStream_t s = (cudaStream_t)stream;
+    return from_cuda(decoder == 0 ? launch_q4_k_dequant_tma(blocks, w_out, nblk, s)
+                                  : launch_q4_k_dequant_general(blocks, w_out, nblk, s));
+}
+
 gai4_status gai4_quantize_x_q8(const float* x, int8_t* xq, float* xd, int64_t K, void* stream) {
     if (!x || !xq || !xd || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xq) || ((uintptr_t)xd & 3u) != 0) return GAI4_ERR_MISALIGNED;

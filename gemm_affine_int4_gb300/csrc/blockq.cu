@@ -31,13 +31,14 @@ constexpr int kXBudget = 64 * 1024; // bytes of staged activations per CTA
 // Q8_0
 // ---------------------------------------------------------------------------
 
-// byte t of w (two's complement code q) -> the float 384 + q:
-// exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80.
+// byte t of w (two's complement code q) -> the float q, exactly: first
+// 384 + q (exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80),
+// then 384 subtracted (exact). Every product q x is exact before it is summed.
 template <int t>
 __device__ __forceinline__ float q8_val(uint32_t w) {
     constexpr int d = 15 - 8 * t;
     const uint32_t v = d >= 0 ? (w << (d >= 0 ? d : 0)) : (w >> (d < 0 ? -d : 0));
-    return __uint_as_float((v & 0x007F8000u) ^ 0x43C00000u);
+    return __uint_as_float((v & 0x007F8000u) ^ 0x43C00000u) - 384.0f;
 }
 
 template <int R>
@@ -119,7 +120,6 @@ __global__ void __launch_bounds__(kNW * 32) q8_0_gemv_kernel(const uint32_t* __r
                     xr[4 * j + 2] = __uint_as_float(v.z);
                     xr[4 * j + 3] = __uint_as_float(v.w);
                 }
-                const float xs = xsum_sm[c];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     float acc = 0.f;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kNW * 32) q8_0_gemv_kernel(const uint32_t* __r
                         acc = fmaf(q8_val<3>(w), xr[4 * i + 3], acc);
                     }
                     const float d = f16_bits_to_f32(wc[r][0]);
-                    part[r] = fmaf(d, fmaf(-384.0f, xs, acc), part[r]);
+                    part[r] = fmaf(d, acc, part[r]);
                 }
             }
         }
@@ -157,13 +157,13 @@ __global__ void __launch_bounds__(kNW * 32) q8_0_gemv_kernel(const uint32_t* __r
 // Q4_K
 // ---------------------------------------------------------------------------
 
-// nibble at bits [p, p+4) of w -> the float 16 + q (exponent of 16, code in
-// mantissa bits 19..22)
+// nibble at bits [p, p+4) of w -> the float q, exactly: first 16 + q
+// (exponent of 16, code in mantissa bits 19..22), then 16 subtracted (exact)
 template <int p>
 __device__ __forceinline__ float q4_val(uint32_t w) {
     constexpr int d = 19 - p;
     const uint32_t v = d >= 0 ? (w << (d >= 0 ? d : 0)) : (w >> (d < 0 ? -d : 0));
-    return __uint_as_float((v & 0x00780000u) | 0x41800000u);
+    return __uint_as_float((v & 0x00780000u) | 0x41800000u) - 16.0f;
 }
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t b0, uint32_t b1, uint32_t b2, int i) {
@@ -312,8 +312,7 @@ __global__ void __launch_bounds__(kNW * 32) q4_k_gemv_kernel(const uint8_t* __re
                     float sc_lo, m_lo, sc_hi, m_hi;
                     q4k_scale_min(hc[r].y, hc[r].z, hc[r].w, j_lo, sc_lo, m_lo);
                     q4k_scale_min(hc[r].y, hc[r].z, hc[r].w, j_lo + 1, sc_hi, m_hi);
-                    const float qx_lo = fmaf(-16.0f, xlo, alo);
-                    const float qx_hi = fmaf(-16.0f, xhi, ahi);
+                    const float qx_lo = alo, qx_hi = ahi;   // sums of exact products q x
                     float v = part[r];
                     v = fmaf(d * sc_lo, qx_lo, v);
                     v = fmaf(-(dmin * m_lo), xlo, v);
@@ -360,7 +359,35 @@ cudaError_t set_smem(KernelT k) {
     return e;
 }
 
+// Test aid: as q4_k_dequant_tma_kernel, with q4k_scale_min, the decoder of
+// q4_k_gemv_kernel
+__global__ void q4_k_dequant_general_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out,
+                                            int64_t nblk) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nblk * 4) return;
+    const int64_t b = t >> 2;
+    const int g = (int)(t & 3);
+    const uint8_t* blk = blocks + b * 144;
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+    float sc_lo, m_lo, sc_hi, m_hi;
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g, sc_lo, m_lo);
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g + 1, sc_hi, m_hi);
+    float* o = out + b * 256 + 64 * g;
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t qb = blk[16 + 32 * g + i];
+        o[i] = fmaf(d * sc_lo, (float)(qb & 15u), -(dmin * m_lo));
+        o[32 + i] = fmaf(d * sc_hi, (float)(qb >> 4), -(dmin * m_hi));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_q4_k_dequant_general(const uint8_t* blocks, float* out, int64_t nblk, cudaStream_t s) {
+    const int64_t threads = nblk * 4;
+    q4_k_dequant_general_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(blocks, out, nblk);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                              cudaStream_t s) {

@@ -26,13 +26,14 @@
 //    which the 32 lanes of a warp read consecutive 16-byte pieces, with the
 //    sum of every 32-element run.
 //  * Decoding places a code in the mantissa of a power of two with one shift
-//    and one three-input logic op. Q8_0: byte b of a word becomes 384 + q
-//    (exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80); sum q x
-//    = sum (384 + q) x - 384 sum x. Q4_K: one shift places the two nibbles of
-//    a byte at mantissa bits 15..18 and 19..22 of 1.0f, giving 1 + q_lo/256
-//    (sub-block 2g) and 1 + q_hi/16 (sub-block 2g + 1); a packed fp32 fma
-//    accumulates both against (x_i, x_{i+32}), starting from (-sum x_lo,
-//    -sum x_hi), so that sum q_lo x = 256 acc.x and sum q_hi x = 16 acc.y.
+//    and one three-input logic op, and one packed fp32 fma turns that float
+//    into the exact code; another adds q x. Q8_0: byte b of a word becomes
+//    384 + q (exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80),
+//    then q = f - 384. Q4_K: one shift places the two nibbles of a byte at
+//    mantissa bits 15..18 and 19..22 of 1.0f, giving 1 + q_lo/256 (sub-block
+//    2g) and 1 + q_hi/16 (sub-block 2g + 1), then (q_lo, q_hi) = (256, 16) f
+//    - (256, 16); the pair accumulates against (x_i, x_{i+32}). Every product
+//    q x is exact before it is summed: a block of zero codes adds exactly 0.
 //  * Per-row results of a set are held in a small shared buffer and combined
 //    over the sets in a fixed order every F row groups (one consumer barrier
 //    per flush, double-buffered): the result does not depend on timing.
@@ -93,6 +94,20 @@ __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo
         : "=f"(d.x), "=f"(d.y)
         : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
     return d;
+}
+// (m_lo * f_lo + c_lo, m_hi * f_hi + c_hi) with every operand a register: the
+// exact codes of a decoded pair
+__device__ __forceinline__ float2 codes2(uint32_t f_lo, uint32_t f_hi, uint32_t m_lo, uint32_t m_hi, uint32_t c_lo,
+                                         uint32_t c_hi) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(f_lo), "r"(f_hi), "r"(m_lo), "r"(m_hi), "r"(c_lo), "r"(c_hi));
+    return d;
+}
+__device__ __forceinline__ float2 fma2q(float2 q, float b_lo, float b_hi, float2 c) {
+    return ffma2(__float_as_uint(q.x), __float_as_uint(q.y), b_lo, b_hi, c);
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -306,6 +321,11 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
     const uint32_t c_mask = pin_reg(FMT == BQ_Q8_0 ? 0x007F8000u : 0x00078000u);
     const uint32_t c_mask2 = pin_reg(0x00780000u);
     const uint32_t c_const = pin_reg(FMT == BQ_Q8_0 ? 0x43C00000u : 0x3F800000u);
+    // code recovery q = m f + c: Q8_0 (1, 1) f + (-384, -384); Q4_K (256, 16) f + (-256, -16)
+    const uint32_t r_m_lo = pin_reg(FMT == BQ_Q8_0 ? 0x3F800000u : 0x43800000u);
+    const uint32_t r_m_hi = pin_reg(FMT == BQ_Q8_0 ? 0x3F800000u : 0x41800000u);
+    const uint32_t r_c_lo = pin_reg(FMT == BQ_Q8_0 ? 0xC3C00000u : 0xC3800000u);
+    const uint32_t r_c_hi = pin_reg(FMT == BQ_Q8_0 ? 0xC3C00000u : 0xC1800000u);
     int slot = s, ph = 0;   // this set's slots: s, s + S, ... (the depth is a multiple of S)
     int buf = 0, fi = 0;
     bool ok = true;
@@ -345,7 +365,6 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                     float4 xv[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) xv[i] = lds128f(xp + (uint32_t)i * 32u * 16u);
-                    const float xsum = sums[ch * 32 + lane];
 #pragma unroll
                     for (int r = 0; r < kR; ++r) {
                         const uint32_t bp = rows + (uint32_t)r * kChunkBytes + 36u * (uint32_t)lane;
@@ -355,12 +374,14 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                         for (int i = 0; i < 8; ++i) {
                             const uint32_t w = lds32(bp + 4u + 4u * (uint32_t)i);
                             const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
-                            acc = ffma2(lop3_andxor(u0, c_mask, c_const), lop3_andxor(u1, c_mask, c_const), xv[i].x,
-                                        xv[i].y, acc);
-                            acc = ffma2(lop3_andxor(u2, c_mask, c_const), lop3_andxor(u3, c_mask, c_const), xv[i].z,
-                                        xv[i].w, acc);
+                            acc = fma2q(codes2(lop3_andxor(u0, c_mask, c_const), lop3_andxor(u1, c_mask, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        xv[i].x, xv[i].y, acc);
+                            acc = fma2q(codes2(lop3_andxor(u2, c_mask, c_const), lop3_andxor(u3, c_mask, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        xv[i].z, xv[i].w, acc);
                         }
-                        part[r] = fmaf(f16_bits_to_f32(hdr), fmaf(-384.0f, xsum, acc.x + acc.y), part[r]);
+                        part[r] = fmaf(f16_bits_to_f32(hdr), acc.x + acc.y, part[r]);
                     }
                 } else if (ch == a.chunks - 1 && a.last_half) {
                     // A last chunk of at most 4 super-blocks (16 items): lanes
@@ -369,7 +390,7 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                     const int sb = it >> 2, g = it & 3;
                     const int sub = 8 * (ch * 8 + sb) + 2 * g;
                     const float sx_lo = sums[sub], sx_hi = sums[sub + 1];
-                    float2 acc = make_float2(-sx_lo, -sx_hi);
+                    float2 acc = make_float2(0.f, 0.f);
                     const uint32_t xp = xs_base + (uint32_t)(ch * 16 * 32 + it) * 16u;
                     const uint32_t rowa = rows + (uint32_t)rr * kChunkBytes;
                     const uint32_t qoff = 144u * (uint32_t)sb + 16u + 32u * (uint32_t)g;
@@ -383,14 +404,18 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                             const float4 p1 = lds128f(xp + (uint32_t)(8 * h + 2 * t + 1) * 32u * 16u);
                             const uint32_t w = wv[t];
                             const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
-                            acc = ffma2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const), p0.x, p0.y,
-                                        acc);
-                            acc = ffma2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const), p0.z, p0.w,
-                                        acc);
-                            acc = ffma2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const), p1.x, p1.y,
-                                        acc);
-                            acc = ffma2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const), p1.z, p1.w,
-                                        acc);
+                            acc = fma2q(codes2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        p0.x, p0.y, acc);
+                            acc = fma2q(codes2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        p0.z, p0.w, acc);
+                            acc = fma2q(codes2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        p1.x, p1.y, acc);
+                            acc = fma2q(codes2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const),
+                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                        p1.z, p1.w, acc);
                         }
                     }
                     const uint4 hdr = lds128(rowa + 144u * (uint32_t)sb);
@@ -398,9 +423,9 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                     float sc_lo, m_lo, sc_hi, m_hi;
                     scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
                     float v = 0.f;
-                    v = fmaf(d * sc_lo, 256.0f * acc.x, v);
+                    v = fmaf(d * sc_lo, acc.x, v);
                     v = fmaf(-(dmin * m_lo), sx_lo, v);
-                    v = fmaf(d * sc_hi, 16.0f * acc.y, v);
+                    v = fmaf(d * sc_hi, acc.y, v);
                     v = fmaf(-(dmin * m_hi), sx_hi, v);
                     static_assert(kR == 2, "the half-chunk mapping pairs the warp's two rows");
                     part[0] += rr == 0 ? v : 0.f;
@@ -412,7 +437,7 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                     const float sx_lo = sums[sub], sx_hi = sums[sub + 1];
                     float2 acc[kR];
 #pragma unroll
-                    for (int r = 0; r < kR; ++r) acc[r] = make_float2(-sx_lo, -sx_hi);
+                    for (int r = 0; r < kR; ++r) acc[r] = make_float2(0.f, 0.f);
                     const uint32_t xp = xs_base + (uint32_t)(ch * 16 * 32 + lane) * 16u;
                     const uint32_t qoff = 144u * (uint32_t)sb + 16u + 32u * (uint32_t)g;
 #pragma unroll
@@ -431,14 +456,18 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                                 const uint32_t w = wv[t];
                                 const float4 p0 = xv[2 * t], p1 = xv[2 * t + 1];
                                 const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
-                                acc[r] = ffma2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const), p0.x,
-                                               p0.y, acc[r]);
-                                acc[r] = ffma2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const), p0.z,
-                                               p0.w, acc[r]);
-                                acc[r] = ffma2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const), p1.x,
-                                               p1.y, acc[r]);
-                                acc[r] = ffma2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const), p1.z,
-                                               p1.w, acc[r]);
+                                acc[r] = fma2q(codes2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const),
+                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                               p0.x, p0.y, acc[r]);
+                                acc[r] = fma2q(codes2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const),
+                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                               p0.z, p0.w, acc[r]);
+                                acc[r] = fma2q(codes2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const),
+                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                               p1.x, p1.y, acc[r]);
+                                acc[r] = fma2q(codes2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const),
+                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
+                                               p1.z, p1.w, acc[r]);
                             }
                         }
                     }
@@ -449,9 +478,9 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                         float sc_lo, m_lo, sc_hi, m_hi;
                         scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
                         float v = part[r];
-                        v = fmaf(d * sc_lo, 256.0f * acc[r].x, v);
+                        v = fmaf(d * sc_lo, acc[r].x, v);
                         v = fmaf(-(dmin * m_lo), sx_lo, v);
-                        v = fmaf(d * sc_hi, 16.0f * acc[r].y, v);
+                        v = fmaf(d * sc_hi, acc[r].y, v);
                         v = fmaf(-(dmin * m_hi), sx_hi, v);
                         part[r] = v;
                     }
@@ -600,7 +629,36 @@ cudaError_t launch_bq(const void* blocks, const float* x, const int8_t* xq, cons
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, wmap, a);
 }
 
+// Test aid: one thread per (super-block, 64-weight group g) writes the group's
+// 64 weights w = d * sc * q - dmin * m (one rounding: d * sc * q and dmin * m
+// are exact in binary32) with the (sc, m) of sub-blocks 2g and 2g + 1 from
+// scale_min_pair, the decoder of q4_k_tma_kernel, reading the 16-byte header
+// as that kernel does.
+__global__ void q4_k_dequant_tma_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out, int64_t nblk) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nblk * 4) return;
+    const int64_t b = t >> 2;
+    const int g = (int)(t & 3);
+    const uint8_t* blk = blocks + b * 144;
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+    float sc_lo, m_lo, sc_hi, m_hi;
+    scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
+    float* o = out + b * 256 + 64 * g;
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t qb = blk[16 + 32 * g + i];
+        o[i] = fmaf(d * sc_lo, (float)(qb & 15u), -(dmin * m_lo));
+        o[32 + i] = fmaf(d * sc_hi, (float)(qb >> 4), -(dmin * m_hi));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_q4_k_dequant_tma(const uint8_t* blocks, float* out, int64_t nblk, cudaStream_t s) {
+    const int64_t threads = nblk * 4;
+    q4_k_dequant_tma_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(blocks, out, nblk);
+    return cudaGetLastError();
+}
 
 // Rows must start on 16-byte boundaries (TMA) and the staged activations must
 // fit in shared memory next to a ring of at least two stages per set.

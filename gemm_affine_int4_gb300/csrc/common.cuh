@@ -50,7 +50,6 @@ struct BF16 {
     // 16-bit magic for the code -> value trick: bit pattern of 128.0 (bf16 has
     // 7 stored mantissa bits, so 128 + q is exact for q < 128)
     static constexpr uint32_t kMagic16 = 0x4300u;
-    static constexpr int kMagicOffset = 128;
     __device__ __forceinline__ static float to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
     __device__ __forceinline__ static uint16_t from_f32(float f) {
         return __bfloat16_as_ushort(__float2bfloat16_rn(f));
@@ -63,7 +62,6 @@ struct F16 {
     static constexpr bool kIsBF16 = false;
     // bit pattern of 1024.0 (10 stored mantissa bits: 1024 + q exact for q < 1024)
     static constexpr uint32_t kMagic16 = 0x6400u;
-    static constexpr int kMagicOffset = 1024;
     __device__ __forceinline__ static float to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
     __device__ __forceinline__ static uint16_t from_f32(float f) { return __half_as_ushort(__float2half_rn(f)); }
 };

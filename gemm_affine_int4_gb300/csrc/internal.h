@@ -105,6 +105,11 @@ cudaError_t launch_q8_0_i8_gemv(const uint32_t* blocks, const int8_t* xq, const 
                                 int64_t K, cudaStream_t s);
 cudaError_t launch_quantize_x_q8(const float* x, int8_t* xq, float* xd, int64_t K, cudaStream_t s);
 
+// Q4_K weights w[b][256] of nblk super-blocks with the (sc, m) decoder of the
+// TMA-staged kernel (blockq_tma.cu) or of the general kernel (blockq.cu): test aid
+cudaError_t launch_q4_k_dequant_tma(const uint8_t* blocks, float* out, int64_t nblk, cudaStream_t s);
+cudaError_t launch_q4_k_dequant_general(const uint8_t* blocks, float* out, int64_t nblk, cudaStream_t s);
+
 // block-quantized GEMVs, general case (blockq.cu)
 cudaError_t launch_q8_0_gemv(const uint32_t* blocks, const float* x, float* out, int64_t N,
                              int64_t K, cudaStream_t s);

@@ -24,11 +24,12 @@
 //  * A code becomes a number through the mantissa of 1.0f: one shift places
 //    two codes at mantissa bits 15..18 and 19..22, and one three-input logic
 //    op each (mask, then the exponent of 1.0f) gives the floats 1 + q/256 and
-//    1 + q/16 exactly. Per 32-bit word of 8 codes: 4 shifts, 8 logic ops and 8
-//    fmas (4 packed fma.rn.f32x2), into an even-code and an odd-code
-//    accumulator that start at
-//    -sum x_even and -sum x_odd of the chunk, so that
-//    256 * acc_even + 16 * acc_odd is the chunk's sum q x.
+//    1 + q/16 exactly; one packed fma (256, 16) * f - (256, 16) turns the pair
+//    into the exact codes (q_even, q_odd), and one more adds q * x into an
+//    (even, odd) accumulator pair. Per 32-bit word of 8 codes: 4 shifts, 8
+//    logic ops and 8 packed fma.rn.f32x2. Every product q x is exact before
+//    it is summed, so a chunk whose codes are all zero adds exactly zero (no
+//    offset is ever subtracted).
 #include <algorithm>
 #include <initializer_list>
 
@@ -71,6 +72,7 @@ struct Qmv4Args {
     uint32_t w_rs, w_is;    // byte strides of a row and of an iteration in a stage's packed weights
     uint32_t sb_rs, sb_is;  // element strides of a row and of an iteration in a stage's scales / biases
     uint32_t mask_lo, mask_hi, one;   // operands of the three-input logic op, kept in registers
+    uint32_t k256, k16, km256, km16;  // 256.0f, 16.0f, -256.0f, -16.0f (code recovery), kept in registers
     int flush;              // row blocks whose partial sums are held in shared memory between flushes
     int* status;
     long long spin_limit;
@@ -83,10 +85,6 @@ __device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t 
     return d;
 }
 
-#ifndef QMV4_PACKED_FMA
-#define QMV4_PACKED_FMA 1
-#endif
-
 // (acc.x + a_lo * b_lo, acc.y + a_hi * b_hi): two binary32 fmas in one instruction
 __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo, float b_hi, float2 c) {
     float2 d;
@@ -94,6 +92,17 @@ __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo
         " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
         : "=f"(d.x), "=f"(d.y)
         : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
+    return d;
+}
+// exact codes from the pair (1 + q_lo/256, 1 + q_hi/16): (256, 16) * f - (256, 16)
+// (every operand a register)
+__device__ __forceinline__ float2 codes2(uint32_t f_lo, uint32_t f_hi, uint32_t k256, uint32_t k16, uint32_t km256,
+                                         uint32_t km16) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(f_lo), "r"(f_hi), "r"(k256), "r"(k16), "r"(km256), "r"(km16));
     return d;
 }
 
@@ -248,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- consumers: main loop ----------------
     const int g = warp / S, sl = warp % S;
     const uint32_t mlo = pin_reg(a.mask_lo), mhi = pin_reg(a.mask_hi), one = pin_reg(a.one);
+    const uint32_t k256 = pin_reg(a.k256), k16 = pin_reg(a.k16), km256 = pin_reg(a.km256), km16 = pin_reg(a.km16);
     const int grp_off = (lane * 32) >> a.gs_log2;   // this lane's group within an iteration
     St* out = static_cast<St*>(a.out);
     int slot = 0, ph = 0;
@@ -278,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&empty[slot]);
 
                 const float4 cst = cs[it * 32 + lane];
-                float2 acc[R];   // (even codes, odd codes)
+                float2 acc[R];   // (even codes, odd codes): sums of exact products q x
 #pragma unroll
-                for (int r = 0; r < R; ++r) acc[r] = make_float2(cst.x, cst.y);
+                for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int tw = 0; tw < 4; ++tw) {
                     const float4 p0 = xs[(it * 8 + 2 * tw) * 32 + lane];
@@ -289,26 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r = 0; r < R; ++r) {
                         const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
                         const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;   // codes (0,1) .. (6,7)
-                        if constexpr (QMV4_PACKED_FMA) {
-                            acc[r] = ffma2(lop3_andor(u0, mlo, one), lop3_andor(u0, mhi, one), p0.x, p0.y, acc[r]);
-                            acc[r] = ffma2(lop3_andor(u1, mlo, one), lop3_andor(u1, mhi, one), p0.z, p0.w, acc[r]);
-                            acc[r] = ffma2(lop3_andor(u2, mlo, one), lop3_andor(u2, mhi, one), p1.x, p1.y, acc[r]);
-                            acc[r] = ffma2(lop3_andor(u3, mlo, one), lop3_andor(u3, mhi, one), p1.z, p1.w, acc[r]);
-                        } else {
-                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u0, mlo, one)), p0.x, acc[r].x);
-                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u0, mhi, one)), p0.y, acc[r].y);
-                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u1, mlo, one)), p0.z, acc[r].x);
-                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u1, mhi, one)), p0.w, acc[r].y);
-                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u2, mlo, one)), p1.x, acc[r].x);
-                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u2, mhi, one)), p1.y, acc[r].y);
-                            acc[r].x = fmaf(__uint_as_float(lop3_andor(u3, mlo, one)), p1.z, acc[r].x);
-                            acc[r].y = fmaf(__uint_as_float(lop3_andor(u3, mhi, one)), p1.w, acc[r].y);
-                        }
+                        float2 q;
+                        q = codes2(lop3_andor(u0, mlo, one), lop3_andor(u0, mhi, one), k256, k16, km256, km16);
+                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p0.x, p0.y, acc[r]);
+                        q = codes2(lop3_andor(u1, mlo, one), lop3_andor(u1, mhi, one), k256, k16, km256, km16);
+                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p0.z, p0.w, acc[r]);
+                        q = codes2(lop3_andor(u2, mlo, one), lop3_andor(u2, mhi, one), k256, k16, km256, km16);
+                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p1.x, p1.y, acc[r]);
+                        q = codes2(lop3_andor(u3, mlo, one), lop3_andor(u3, mhi, one), k256, k16, km256, km16);
+                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p1.z, p1.w, acc[r]);
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float qx = fmaf(256.f, acc[r].x, 16.f * acc[r].y);   // sum q x of the chunk
+                    const float qx = acc[r].x + acc[r].y;   // sum q x of the chunk
                     part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.z, part[r]));
                 }
             } else {
@@ -537,6 +541,10 @@ cudaError_t launch_qmv4(const uint32_t* w, const void* scales, const void* biase
     a.mask_lo = kMaskLo;
     a.mask_hi = kMaskHi;
     a.one = kOne;
+    a.k256 = 0x43800000u;    // 256.0f
+    a.k16 = 0x41800000u;     // 16.0f
+    a.km256 = 0xC3800000u;   // -256.0f
+    a.km16 = 0xC1800000u;    // -16.0f
     a.status = status;
     a.spin_limit = spin_limit;
     switch (dtype) {

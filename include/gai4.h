@@ -264,6 +264,19 @@ gai4_status gai4_q4_k_gemv(const uint8_t* blocks, const float* x, float* out,
                            int64_t N, int64_t K, void* stream);
 
 /*
+ * gai4_q4_k_dequantize -- test aid for the Q4_K 6-bit scale / min decoding
+ * (hanzo-kernel quant.rs, Q4_K section, get_scale_min_k4): the weights of N x
+ * K/256 super-blocks laid out as for gai4_q4_k_gemv,
+ *   w_out[n, k] = RN_f32(d * sc_j * q - dmin * m_j)   (float32 [N, K], device)
+ * (one rounding: d * sc_j * q and dmin * m_j are exact in binary32), with
+ * (sc_j, m_j) decoded by the same device function as a GEMV kernel:
+ * decoder 0 = the TMA-staged kernel's, 1 = the general kernel's.
+ * K a multiple of 256; blocks 16-byte aligned, w_out 4-byte aligned.
+ */
+gai4_status gai4_q4_k_dequantize(const uint8_t* blocks, float* w_out, int64_t N, int64_t K, int decoder,
+                                 void* stream);
+
+/*
  * gai4_q8_0_34b_gemv -- Q8_0 matrix-vector product over GGUF's own 34-byte
  * block (hanzo-kernel quant.rs describes its nine-word "production layout" as
  * a re-packing of this block; the byte layout itself is read from the GGUF

@@ -155,3 +155,30 @@ def test_qmv_repeatable():
     a = g4.gai4_qmv(*args)
     c = g4.gai4_qmv(*args)
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+@pytest.mark.parametrize("gs", [32, 64, 128])
+@pytest.mark.parametrize("bits", [2, 3, 6, 8])
+def test_width_sweep_full_size_sampled(bits, gs, full_weights):
+    """The bit-width x group-size sweep at N = K = 4096 for M in {1, 8, 64},
+    bf16, in the launch configuration the benchmark times (qmv for M = 1,
+    qmm_t with automatic plan and a workspace otherwise), on sampled rows."""
+    N = K = 4096
+    W = full_weights(N, K, 0)
+    packed, s, b = oracle.quantize(W, bits, gs, "bf16")
+    pg, sg, bg = g4.gai4_quantize(to_dev(W), bits, gs, torch.bfloat16)
+    assert np.array_equal(pg.cpu().view(torch.int32).numpy().view(np.uint32), packed)
+    rows = sample_rows(N, 48, bits * 1000 + gs)
+    for M in (1, 8, 64):
+        x = synth.activations(M, K, "bf16", 4100 + M)
+        xd = to_dev(x, "bf16")
+        if M == 1:
+            out = g4.gai4_qmv(pg, sg, bg, xd.reshape(-1), bits=bits, group_size=gs).reshape(1, N)
+        else:
+            nbytes = g4.gai4_qmm_t_workspace_bytes(M, N, K, bits, gs, torch.bfloat16, 0)
+            ws = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device="cuda")
+            out = g4.gai4_qmm_t(pg, sg, bg, xd, bits=bits, group_size=gs, split_k=0, workspace=ws)
+        got = to_host_f64(out, "bf16")
+        assert np.all(np.isfinite(got))
+        ref, absdot = oracle.qmm(packed, s, b, x, bits, gs, "bf16", rows=rows)
+        assert_within(got[:, rows], ref, absdot, "bf16", f"bits={bits} gs={gs} M={M}")

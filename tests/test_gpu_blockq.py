@@ -117,3 +117,49 @@ def test_blockq_full_size_sampled(kind, N, K, seed):
         ref, absdot = oracle.q4_k_gemv(blocks, x, rows=rows)
     assert_within(got[rows], ref, absdot, "f32", f"{kind} {N}x{K}")
     assert np.all(np.isfinite(got))
+
+
+def _q4k_enumerated_blocks(seed: int) -> np.ndarray:
+    """8 x 4096 super-blocks: for each sub-block j and each (sc, m) in 64 x 64,
+    one block whose 12 scale bytes give pair j = (sc, m) under get_scale_min_k4
+    (the other bits of those bytes random); d = dmin = 1.0 (f16), random codes."""
+    r = synth.rng(seed)
+    sc, m = np.meshgrid(np.arange(64), np.arange(64), indexing="ij")
+    sc, m = sc.reshape(-1), m.reshape(-1)
+    out = []
+    for j in range(8):
+        blk = r.integers(0, 256, size=(4096, 144), dtype=np.uint8)
+        blk[:, 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+        blk[:, 2:4] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+        s = blk[:, 4:16].astype(np.int64)
+        if j < 4:
+            s[:, j] = (s[:, j] & 0xC0) | sc
+            s[:, j + 4] = (s[:, j + 4] & 0xC0) | m
+        else:
+            s[:, j + 4] = (sc & 15) | ((m & 15) << 4)
+            s[:, j - 4] = (s[:, j - 4] & 0x3F) | ((sc >> 4) << 6)
+            s[:, j] = (s[:, j] & 0x3F) | ((m >> 4) << 6)
+        blk[:, 4:16] = s.astype(np.uint8)
+        out.append(blk)
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("decoder", [0, 1])
+def test_q4_k_scale_min_decode_bit_exact(decoder):
+    """The 6-bit (sc, m) decoding of both Q4_K kernels, through the test-aid
+    dequantize that runs the kernel's own decoder: every (sc, m) pair for
+    every sub-block j, then 1e5 random super-blocks; every weight must equal
+    the oracle's binary64 value rounded once to binary32."""
+    enum = _q4k_enumerated_blocks(500)
+    rnd = synth.q4_k_blocks(100000, 256, 501).reshape(-1, 144)
+    for name, blocks in (("enumerated", enum), ("random", rnd)):
+        nb = blocks.shape[0]
+        got = g4.gai4_q4_k_dequantize(to_dev(blocks.reshape(nb, 1, 144)), decoder).cpu().numpy()
+        want = np.stack([oracle.q4_k_dequant_block(blocks[b]) for b in range(nb)]).astype(np.float32)
+        assert np.all(np.isfinite(want))
+        bad = np.flatnonzero(got.reshape(-1).view(np.uint32) != want.reshape(-1).view(np.uint32))
+        assert bad.size == 0, (name, decoder, bad[:8], got.reshape(-1)[bad[:8]], want.reshape(-1)[bad[:8]])
+    # the enumerated blocks really cover every (sc, m) of every j
+    for j in range(8):
+        pairs = {oracle.q4_k_scale_min(enum[b, 4:16], j) for b in range(j * 4096, (j + 1) * 4096)}
+        assert len(pairs) == 4096, j

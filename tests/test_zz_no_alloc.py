@@ -1,10 +1,13 @@
 """gai4_qmm_t_noalloc: the split-K matmul for callers that cannot allocate
-device memory (its partials live in the library's fixed 8 MiB device array).
+device memory (its fp32 partials live in the library's fixed 8 MiB device
+array).
 
-Called through the C ABI and checked against gai4_qmm_t (caller-provided
-workspace) on two calls in a row with different shapes, so the second call
-runs on the array as the first left it. Collected last (file name) so that a
-run stopping at the first failure has already run every other test.
+Called through the C ABI on two calls in a row with different shapes, so the
+second call runs on the array as the first left it. Each output must equal
+gai4_qmm_t with a caller-provided workspace of the array's size (hence the
+same automatic split) bit for bit, since a fixed split sums in a fixed order,
+and must meet the oracle bound. Collected last (file name) so that a run
+stopping at the first failure has already run every other test.
 """
 import ctypes
 
@@ -33,21 +36,24 @@ def _noalloc_c(packed, s, b, x, out, split_k):
 
 
 def test_noalloc_matches_qmm_t_two_calls():
-    shapes = [(1000, 4096, 33), (2048, 10752, 85)]    # (N, K, M): the second needs more partials
+    # (N, K, M): the second needs more partials than the first
+    shapes = [(1000, 4096, 33), (2048, 10752, 85)]
     for i, (N, K, M) in enumerate(shapes):
         _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=900 + i)
         P, S_, B_, X = to_dev(packed), to_dev(s, "bf16"), to_dev(b, "bf16"), to_dev(x, "bf16")
         path, splits = g4.gai4_qmm_t_plan(M, N, K, 4, 64, torch.bfloat16, 0, g4.NOALLOC_SCRATCH_BYTES)
         assert path == 1 and splits > 1        # the scratch array is really used
+        assert splits * M * N * 4 <= g4.NOALLOC_SCRATCH_BYTES
+        assert g4.gai4_qmm_t_workspace_bytes(M, N, K, 4, 64, torch.bfloat16, splits) > 0
         out_na = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         assert _noalloc_c(P, S_, B_, X, out_na, 0) == 0
-        ws = torch.empty(splits * M * N, dtype=torch.float32, device="cuda")
-        out_ref = g4.gai4_qmm_t(P, S_, B_, X, bits=4, group_size=64, split_k=splits, workspace=ws)
+        # the same automatic plan: a caller workspace as large as the array
+        ws = torch.empty(g4.NOALLOC_SCRATCH_BYTES // 4, dtype=torch.float32, device="cuda")
+        out_ref = g4.gai4_qmm_t(P, S_, B_, X, bits=4, group_size=64, split_k=0, workspace=ws)
         assert g4.gai4_last_device_status() == 0
-        _, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16")
-        got = to_host_f64(out_na, "bf16")
-        assert np.all(np.isfinite(got))
-        assert_within(got, to_host_f64(out_ref, "bf16"), absdot, "bf16", f"noalloc call {i + 1}")
+        assert torch.equal(out_na, out_ref), f"noalloc call {i + 1} differs from gai4_qmm_t"
+        ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16")
+        assert_within(to_host_f64(out_na, "bf16"), ref, absdot, "bf16", f"noalloc call {i + 1} vs oracle")
 
 
 def test_noalloc_rejects_oversized_split():

@@ -3,9 +3,12 @@
 Per output element (stated for the method's outputs):
     |gpu - oracle| <= 1e-3 * sum_k |w_hat[n,k] * x[m,k]| + ulp_T(oracle)
 where ulp_T(v) is the spacing of the output dtype T at max(|v|, smallest
-normal of T). The relative term covers binary32 accumulation in any order
-(and the single rounding of each dequantized weight to the 16-bit MMA operand
-type on the tensor-core path); the ulp term covers the final rounding to T.
+normal of T). The relative term covers binary32 accumulation in any order;
+the ulp term covers the final rounding to T. The tensor-core path also rounds
+each dequantized weight once to the 16-bit MMA operand type (unit roundoff
+2^-8 for bf16): on ordinary rows the output ulp covers that, and a crafted row
+whose operand errors add coherently while its output cancels departs from this
+bound (tests/test_gpu_zero_rows.py pins that case and its own bound).
 """
 import numpy as np
 
