@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -411,6 +412,25 @@ def kernel_launches_per_step(g4, calls, torch):
     return n
 
 
+def inner_reps(torch, stream, one_step, K, args):
+    """Replays of the step per timed step: --inner if given, else enough that
+    the K timed steps span at least --min-timed-s seconds (estimated from a few
+    untimed replays), so that the clock sampler sees the timed region."""
+    if args.inner > 0:
+        return args.inner
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = 10
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            one_step()
+        e1.record(stream)
+    stream.synchronize()
+    step_ms = max(e0.elapsed_time(e1) / n, 1e-3)
+    return max(1, int(math.ceil(args.min_timed_s * 1e3 / (max(K, 1) * step_ms))))
+
+
 def max_over_ranks(torch, dist, x, device):
     """The slowest rank's value (every rank gets it): the job's step time."""
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
@@ -484,6 +504,9 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
     K = args.steps
+    reps = inner_reps(torch, stream, one_step, K, args)
+    if world > 1:   # every rank replays the same number of steps
+        reps = int(max_over_ranks(torch, dist, reps, dev))
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fams]
           for _ in range(K)]
     t0 = torch.cuda.Event(enable_timing=True)
@@ -498,7 +521,6 @@ def run_gpu(args, rank, world, local_rank):
     time.sleep(0.3)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        reps = max(1, args.inner)
         for k in range(K):
             for _ in range(reps):
                 one_step()
@@ -564,6 +586,7 @@ def run_gpu(args, rank, world, local_rank):
             "l2": "no flush: %.0f MB of distinct weights per step > 129 MB L2" % (total_bytes / 1e6),
             "timing": "the step is one CUDA graph (kernels chained by programmatic dependent launch), "
                       "CUDA events on the launching stream; the breakdown replays one graph per family",
+            "replays_per_timed_step": reps, "timed_region_s": round(elapsed_ms / 1e3, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "breakdown": {fam: {"ms": round(fam_ms[fam], 5), "GB/s": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9, 1),
@@ -865,7 +888,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--inner", type=int, default=1, help="untimed-event steps per timed step")
+    ap.add_argument("--inner", type=int, default=0,
+                    help="step replays per timed step (0: enough for --min-timed-s seconds in all)")
+    ap.add_argument("--min-timed-s", type=float, default=1.0)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

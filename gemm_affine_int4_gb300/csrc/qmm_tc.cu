@@ -823,9 +823,12 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     }
 
     // scales / biases: 16-bit [N, K / group_size], box {8 groups, 128 rows}
-    // (16-byte rows, no swizzle); the row stride must be a multiple of 16 bytes
+    // (16-byte rows, no swizzle); the row stride and both base addresses must
+    // be multiples of 16 bytes, otherwise the dequantize warps load them from
+    // global memory
     const int64_t groups = K / L.group_size;
-    const bool sbt = groups % 8 == 0;
+    const bool sbt = groups % 8 == 0 && (reinterpret_cast<uintptr_t>(L.scales) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(L.biases) & 15u) == 0;
     memset(&smap, 0, sizeof(smap));
     memset(&bmap, 0, sizeof(bmap));
     if (sbt) {

@@ -128,11 +128,10 @@ gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* b
  * automatic mode the split is also limited to what `workspace_bytes` holds
  * (workspace may be NULL: no split). The summation order is fixed, so a
  * given split gives bit-identical results run to run.
- * On the tensor-core path with K / group_size a multiple of 8, scales and
- * biases are fetched by TMA and their base pointers must be 16-byte aligned;
- * otherwise the call returns GAI4_ERR_CUDA and launches nothing. (Whole
- * tensors from an allocator always are; gai4_qmv has a fallback for any
- * alignment.)
+ * On the tensor-core path scales and biases are fetched by TMA with the
+ * packed weights when K / group_size is a multiple of 8 and both base
+ * pointers are 16-byte aligned, and read from global memory by the
+ * dequantizing threads otherwise (any 2-byte aligned pointer works).
  */
 gai4_status gai4_qmm_t(const uint32_t* w_packed, const void* scales, const void* biases,
                        const void* x, void* out, gai4_dtype dtype, int bits, int group_size,

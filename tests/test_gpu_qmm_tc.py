@@ -113,3 +113,30 @@ def test_tc_large_m_sampled(N, K, M):
     rows = sample_rows(N, 24, M)
     ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16", rows=rows)
     assert_within(got[:, rows], ref, absdot, "bf16", f"qmm_t large M {K}x{N} M={M}")
+
+
+@pytest.mark.parametrize("offset", [1, 3])   # scales / biases 2 and 6 bytes past a 16-byte boundary
+def test_tc_misaligned_scales_biases(offset):
+    """Scale / bias pointers that are not 16-byte aligned (views into a larger
+    buffer) take the global-load path of the dequantize warps: same result
+    bits as with aligned copies, and within the bound of the oracle."""
+    N, K, M = 256, 2048, 24
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=77 + offset)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16")
+    sd, bd = to_dev(s, "bf16"), to_dev(b, "bf16")
+    sbig = torch.empty(sd.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    bbig = torch.empty(bd.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    s_mis = sbig[offset:offset + sd.numel()].view(sd.shape)
+    b_mis = bbig[offset:offset + bd.numel()].view(bd.shape)
+    s_mis.copy_(sd)
+    b_mis.copy_(bd)
+    assert s_mis.data_ptr() % 16 != 0 and b_mis.data_ptr() % 16 != 0
+    assert g4.gai4_qmm_t_plan(M, N, K, 4, 64, torch.bfloat16)[0] == 1
+    wd, xd = to_dev(packed), to_dev(x, "bf16")
+    for S in (1, 2):
+        ws = torch.empty(1 << 20, dtype=torch.float32, device="cuda")
+        out_a = g4.gai4_qmm_t(wd, sd, bd, xd, bits=4, group_size=64, split_k=S, workspace=ws)
+        out_m = g4.gai4_qmm_t(wd, s_mis, b_mis, xd, bits=4, group_size=64, split_k=S, workspace=ws)
+        assert g4.gai4_last_device_status() == 0
+        assert torch.equal(out_a, out_m)
+        assert_within(to_host_f64(out_m, "bf16"), ref, absdot, "bf16", f"misaligned scales S={S}")
