@@ -19,17 +19,31 @@
 //    3-D TMA box per tensor brings a whole stage; otherwise one 2-D box per
 //    iteration (zero fill past K). Consumer lanes issue no copies and no
 //    global loads in the loop.
-//  * x is staged once per CTA in binary32, permuted so that a warp's 16-byte
-//    reads are contiguous, with per-chunk sums for the bias term.
-//  * A code becomes a number through the mantissa of 1.0f: one shift places
-//    two codes at mantissa bits 15..18 and 19..22, and one three-input logic
-//    op each (mask, then the exponent of 1.0f) gives the floats 1 + q/256 and
-//    1 + q/16 exactly; one packed fma (256, 16) * f - (256, 16) turns the pair
-//    into the exact codes (q_even, q_odd), and one more adds q * x into an
-//    (even, odd) accumulator pair. Per 32-bit word of 8 codes: 4 shifts, 8
-//    logic ops and 8 packed fma.rn.f32x2. Every product q x is exact before
-//    it is summed, so a chunk whose codes are all zero adds exactly zero (no
-//    offset is ever subtracted).
+//  * x is staged once per CTA, permuted so that a warp's 16-byte reads are
+//    contiguous, with per-chunk sums for the bias term: 16-bit activations
+//    as pairs (x_j, x_{j+4}) of the same type, binary32 ones as they are.
+//  * Every product q x is exact before it is summed, so a chunk whose codes
+//    are all zero adds exactly zero (no offset is ever subtracted).
+//    16-bit activations: a 16-bit value whose exponent field is 0 or 1 is
+//    its low 8 bits times the smallest subnormal (2^-133 in bf16, 2^-24 in
+//    f16), so one AND of a word with 0x000F000F gives the pair
+//    (q_0, q_4) * 2^-e and one with 0x00F000F0 the pair (q_1, q_5) * 2^-e * 16,
+//    exactly, and the same on the word shifted by 8 gives codes 2, 6 and 3, 7.
+//    Each half feeds one mixed-precision fma (binary32 += a * b, both factors
+//    16-bit, the product exact) into one of two accumulators per row (codes
+//    in bits 0..3 or 4..7 of a half), joined as a + b / 16. Per word
+//    of 8 codes: 1 shift, 4 ANDs, 8 fmas. The f16 products (at least 2^-48 in
+//    magnitude) are
+//    binary32 normals; for bf16 each 32-element chunk of x is scaled by a
+//    power of two 2^k that puts its largest magnitude in [2^127, 2^128), so
+//    the products are binary32 normals down to 2^-120 of that magnitude, and
+//    the chunk's code sum is scaled back by 2^(133-k).
+//    binary32 activations: code j of a word sits at bits 4j..4j+3 (j < 5)
+//    or, after one 12-bit shift, at bits 8.., 12.., 16..; one logic op ORs it
+//    into a float of exponent 23 - (its bit position), i.e. 2^e + q exactly;
+//    a packed add of (-2^e0, -2^e1) gives the exact pair and a packed fma
+//    adds q * x. Per word: 1 shift, 8 logic ops, 4 packed adds, 4 packed
+//    fmas (fma.rn.f32x2).
 #include <algorithm>
 #include <initializer_list>
 
@@ -50,9 +64,6 @@ constexpr int kCWarps = QMV4_CWARPS;               // consumer warps
 constexpr int kThreads = 32 * (kCWarps + 1);       // + one producer warp
 constexpr int kItCols = 1024;                      // columns of one warp iteration (32 lanes x 32 codes)
 constexpr int kMaxDepth = 8;
-constexpr uint32_t kOne = 0x3F800000u;             // 1.0f
-constexpr uint32_t kMaskLo = 0x00078000u;          // code at mantissa bits 15..18 -> 1 + q/256
-constexpr uint32_t kMaskHi = 0x00780000u;          // code at mantissa bits 19..22 -> 1 + q/16
 
 struct Qmv4Args {
     const void* x;
@@ -71,8 +82,6 @@ struct Qmv4Args {
     int box3;               // 1: one 3-D box per tensor and stage, layout [row][iteration][...]
     uint32_t w_rs, w_is;    // byte strides of a row and of an iteration in a stage's packed weights
     uint32_t sb_rs, sb_is;  // element strides of a row and of an iteration in a stage's scales / biases
-    uint32_t mask_lo, mask_hi, one;   // operands of the three-input logic op, kept in registers
-    uint32_t k256, k16, km256, km16;  // 256.0f, 16.0f, -256.0f, -16.0f (code recovery), kept in registers
     int flush;              // row blocks whose partial sums are held in shared memory between flushes
     int* status;
     long long spin_limit;
@@ -94,16 +103,30 @@ __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo
         : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
     return d;
 }
-// exact codes from the pair (1 + q_lo/256, 1 + q_hi/16): (256, 16) * f - (256, 16)
-// (every operand a register)
-__device__ __forceinline__ float2 codes2(uint32_t f_lo, uint32_t f_hi, uint32_t k256, uint32_t k16, uint32_t km256,
-                                         uint32_t km16) {
+// (a_lo + b_lo, a_hi + b_hi): exact codes from the floats 2^e + q (every operand a register)
+__device__ __forceinline__ float2 fadd2(uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi) {
     float2 d;
-    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
-        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n add.rn.f32x2 d, a, b;\n"
+        " mov.b64 {%0, %1}, d;\n}"
         : "=f"(d.x), "=f"(d.y)
-        : "r"(f_lo), "r"(f_hi), "r"(k256), "r"(k16), "r"(km256), "r"(km16));
+        : "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi));
     return d;
+}
+
+// acc + q.lo * x.lo + q.hi * x.hi: a binary32 accumulator, 16-bit factors
+// (mixed-precision fma: each product exact, one rounding per fma)
+template <bool BF>
+__device__ __forceinline__ void mfma2(uint32_t q2, uint32_t x2, float& acc) {
+    if constexpr (BF)
+        asm("{\n .reg .b16 ql, qh, xl, xh;\n mov.b32 {ql, qh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.bf16 %0, ql, xl, %0;\n fma.rn.f32.bf16 %0, qh, xh, %0;\n}"
+            : "+f"(acc)
+            : "r"(q2), "r"(x2));
+    else
+        asm("{\n .reg .b16 ql, qh, xl, xh;\n mov.b32 {ql, qh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.f16 %0, ql, xl, %0;\n fma.rn.f32.f16 %0, qh, xh, %0;\n}"
+            : "+f"(acc)
+            : "r"(q2), "r"(x2));
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
@@ -120,8 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int n_it = a.n_it, D = a.depth, S = a.S, n_st = a.n_st;
     const int G = kCWarps / S, BR = G * R;
-    float4* xs = reinterpret_cast<float4*>(smem);                     // [n_it][8][32] permuted x
-    float4* cs = xs + (size_t)n_it * 256;                             // [n_it * 32] chunk constants
+    constexpr int kXP = T::kBytes == 4 ? 8 : 4;                       // 16-byte x pieces per lane and iteration
+    uint4* xs = reinterpret_cast<uint4*>(smem);                       // [n_it][kXP][32] permuted x
+    float4* cs = reinterpret_cast<float4*>(xs + (size_t)n_it * kXP * 32);   // [n_it * 32] (sum x, 2^a, 2^b, 0)
     uint8_t* ring = reinterpret_cast<uint8_t*>(cs + (size_t)n_it * 32);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)D * a.stage_bytes);
     uint64_t* empty = full + kMaxDepth;
@@ -213,51 +237,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- consumers: stage x once ----------------
-    // a thread takes 8 consecutive elements (a quarter of a 32-element chunk);
-    // the 4 quarters of a chunk sit in 4 adjacent lanes and add their sums
-    // with shuffles
+    // a thread takes 8 consecutive elements (word qq of a 32-element chunk);
+    // the 4 words of a chunk sit in 4 adjacent lanes and add their sums with
+    // shuffles
     const St* xg = static_cast<const St*>(a.x);
     const int64_t K = a.K;
     for (int u = threadIdx.x; u < n_it * 128; u += kCWarps * 32) {   // n_it * 128 is a multiple of 32
         const int c = u >> 2, qq = u & 3;
         const int64_t k0 = (int64_t)u * 8;
         float v[8];
-        if (k0 < K) {   // K is a multiple of 32: a chunk is all in or all out
-            if constexpr (T::kBytes == 4) {
-                const float4 f0 = *reinterpret_cast<const float4*>(xg + k0);
-                const float4 f1 = *reinterpret_cast<const float4*>(xg + k0 + 4);
-                v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
-                v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
-            } else {
-                const uint4 q = *reinterpret_cast<const uint4*>(xg + k0);
-                const uint32_t uu[4] = {q.x, q.y, q.z, q.w};
+        if constexpr (T::kBytes == 4) {
+            float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+            if (k0 < K) {   // K is a multiple of 32: a chunk is all in or all out
+                f0 = *reinterpret_cast<const float4*>(xg + k0);
+                f1 = *reinterpret_cast<const float4*>(xg + k0 + 4);
+            }
+            v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+            v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+            xs[((c >> 5) * 8 + 2 * qq) * 32 + (c & 31)] = make_uint4(__float_as_uint(f0.x), __float_as_uint(f0.y),
+                                                                     __float_as_uint(f0.z), __float_as_uint(f0.w));
+            xs[((c >> 5) * 8 + 2 * qq + 1) * 32 + (c & 31)] = make_uint4(
+                __float_as_uint(f1.x), __float_as_uint(f1.y), __float_as_uint(f1.z), __float_as_uint(f1.w));
+        } else {
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (k0 < K) q = *reinterpret_cast<const uint4*>(xg + k0);
+            uint32_t uu[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[2 * h] = T::to_f32((uint16_t)(uu[h] & 0xFFFFu));
+                v[2 * h + 1] = T::to_f32((uint16_t)(uu[h] >> 16));
+            }
+            if constexpr (T::kIsBF16) {
+                // chunk scale 2^k: the largest magnitude's exponent field E -> 254
+                uint32_t mb = 0u;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) mb = max(mb, max(uu[h] & 0x7FFFu, (uu[h] >> 16) & 0x7FFFu));
+                mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                const int E = max((int)(mb >> 7), 1);                // subnormal or zero chunk: as E = 1
+                const int k = max(254 - E, 0);                        // Inf / NaN: no scaling
+                const float s1 = __uint_as_float((uint32_t)(127 + (k >> 1)) << 23);
+                const float s2 = __uint_as_float((uint32_t)(127 + k - (k >> 1)) << 23);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    v[2 * h] = T::to_f32((uint16_t)(uu[h] & 0xFFFFu));
-                    v[2 * h + 1] = T::to_f32((uint16_t)(uu[h] >> 16));
+                    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn((v[2 * h] * s1) * s2));
+                    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn((v[2 * h + 1] * s1) * s2));
+                    uu[h] = lo | (hi << 16);
                 }
+                if (qq == 0) {
+                    const int p = 133 - k;                            // the code sum is scaled back by 2^p
+                    cs[c].y = __uint_as_float((uint32_t)(127 + (p >> 1)) << 23);
+                    cs[c].z = __uint_as_float((uint32_t)(127 + p - (p >> 1)) << 23);
+                }
+            } else if (qq == 0) {
+                cs[c].y = 16777216.f;   // 2^24
+                cs[c].z = 1.f;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.f;
+            // pairs (x_j, x_{j+4}), j = 0..3, the order of the decoded code pairs
+            xs[((c >> 5) * 4 + qq) * 32 + (c & 31)] =
+                make_uint4(__byte_perm(uu[0], uu[2], 0x5410), __byte_perm(uu[0], uu[2], 0x7632),
+                           __byte_perm(uu[1], uu[3], 0x5410), __byte_perm(uu[1], uu[3], 0x7632));
         }
-        xs[((c >> 5) * 8 + 2 * qq) * 32 + (c & 31)] = make_float4(v[0], v[1], v[2], v[3]);
-        xs[((c >> 5) * 8 + 2 * qq + 1) * 32 + (c & 31)] = make_float4(v[4], v[5], v[6], v[7]);
-        // chunk sums in a fixed order: quarters (0 + 1) + (2 + 3)
-        float xe = (v[0] + v[2]) + (v[4] + v[6]);
-        float xo = (v[1] + v[3]) + (v[5] + v[7]);
-        xe += __shfl_xor_sync(0xffffffffu, xe, 1);
-        xo += __shfl_xor_sync(0xffffffffu, xo, 1);
-        xe += __shfl_xor_sync(0xffffffffu, xe, 2);
-        xo += __shfl_xor_sync(0xffffffffu, xo, 2);
-        if (qq == 0) cs[c] = make_float4(-xe, -xo, xe + xo, 0.f);
+        // chunk sum (unscaled x) in a fixed order
+        float xsum = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+        if (qq == 0) {
+            cs[c].x = xsum;
+            cs[c].w = 0.f;
+            if constexpr (T::kBytes == 4) {
+                cs[c].y = 1.f;
+                cs[c].z = 1.f;
+            }
+        }
     }
     consumer_bar();
 
     // ---------------- consumers: main loop ----------------
     const int g = warp / S, sl = warp % S;
-    const uint32_t mlo = pin_reg(a.mask_lo), mhi = pin_reg(a.mask_hi), one = pin_reg(a.one);
-    const uint32_t k256 = pin_reg(a.k256), k16 = pin_reg(a.k16), km256 = pin_reg(a.km256), km16 = pin_reg(a.km16);
+    // operands of the logic ops and exact subtractions, kept in registers
+    constexpr bool kBF = T::kBytes == 2 && T::kIsBF16;
+    const uint32_t m2 = pin_reg(0x000F000Fu), mh2 = pin_reg(0x00F000F0u);
+    // binary32: masks of code bits 0.., 4.., 8.., 12.., 16.. and the floats 2^23, 2^19, 2^15, 2^11, 2^7
+    const uint32_t f0 = pin_reg(0xFu), f1 = pin_reg(0xF0u), f2 = pin_reg(0xF00u), f3 = pin_reg(0xF000u),
+                   f4 = pin_reg(0xF0000u);
+    const uint32_t e23 = pin_reg(0x4B000000u), e19 = pin_reg(0x49000000u), e15 = pin_reg(0x47000000u),
+                   e11 = pin_reg(0x45000000u), e7 = pin_reg(0x43000000u);
+    const uint32_t n23 = pin_reg(0xCB000000u), n19 = pin_reg(0xC9000000u), n15 = pin_reg(0xC7000000u),
+                   n11 = pin_reg(0xC5000000u), n7 = pin_reg(0xC3000000u);
     const int grp_off = (lane * 32) >> a.gs_log2;   // this lane's group within an iteration
     St* out = static_cast<St*>(a.out);
     int slot = 0, ph = 0;
@@ -287,33 +354,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
 
-                const float4 cst = cs[it * 32 + lane];
-                float2 acc[R];   // (even codes, odd codes): sums of exact products q x
+                const float4 cst = cs[it * 32 + lane];   // (sum x, 2^a, 2^b): sum q x = code sum * 2^a * 2^b
+                float2 acc[R];   // per row: codes in bits 0..3 (x) and 4..7 (y) of a half
 #pragma unroll
                 for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int tw = 0; tw < 4; ++tw) {
-                    const float4 p0 = xs[(it * 8 + 2 * tw) * 32 + lane];
-                    const float4 p1 = xs[(it * 8 + 2 * tw + 1) * 32 + lane];
+                    if constexpr (T::kBytes == 2) {
+                        const uint4 xp = xs[(it * 4 + tw) * 32 + lane];   // (x_j, x_{j+4}), j = 0..3
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
-                        const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;   // codes (0,1) .. (6,7)
-                        float2 q;
-                        q = codes2(lop3_andor(u0, mlo, one), lop3_andor(u0, mhi, one), k256, k16, km256, km16);
-                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p0.x, p0.y, acc[r]);
-                        q = codes2(lop3_andor(u1, mlo, one), lop3_andor(u1, mhi, one), k256, k16, km256, km16);
-                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p0.z, p0.w, acc[r]);
-                        q = codes2(lop3_andor(u2, mlo, one), lop3_andor(u2, mhi, one), k256, k16, km256, km16);
-                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p1.x, p1.y, acc[r]);
-                        q = codes2(lop3_andor(u3, mlo, one), lop3_andor(u3, mhi, one), k256, k16, km256, km16);
-                        acc[r] = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), p1.z, p1.w, acc[r]);
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
+                            const uint32_t w8 = w >> 8;
+                            mfma2<kBF>(w & m2, xp.x, acc[r].x);    // codes 0, 4
+                            mfma2<kBF>(w & mh2, xp.y, acc[r].y);   // codes 1, 5 (times 16)
+                            mfma2<kBF>(w8 & m2, xp.z, acc[r].x);   // codes 2, 6
+                            mfma2<kBF>(w8 & mh2, xp.w, acc[r].y);  // codes 3, 7 (times 16)
+                        }
+                    } else {
+                        const uint4 p0 = xs[(it * 8 + 2 * tw) * 32 + lane];
+                        const uint4 p1 = xs[(it * 8 + 2 * tw + 1) * 32 + lane];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
+                            const uint32_t h = w >> 12;   // codes 5, 6, 7 at bits 8.., 12.., 16..
+                            float2 q;
+                            q = fadd2(lop3_andor(w, f0, e23), lop3_andor(w, f1, e19), n23, n19);
+                            float2 a2 = acc[r];
+                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p0.x),
+                                       __uint_as_float(p0.y), a2);
+                            q = fadd2(lop3_andor(w, f2, e15), lop3_andor(w, f3, e11), n15, n11);
+                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p0.z),
+                                       __uint_as_float(p0.w), a2);
+                            q = fadd2(lop3_andor(w, f4, e7), lop3_andor(h, f2, e15), n7, n15);
+                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p1.x),
+                                       __uint_as_float(p1.y), a2);
+                            q = fadd2(lop3_andor(h, f3, e11), lop3_andor(h, f4, e7), n11, n7);
+                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p1.z),
+                                       __uint_as_float(p1.w), a2);
+                            acc[r] = a2;
+                        }
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float qx = acc[r].x + acc[r].y;   // sum q x of the chunk
-                    part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.z, part[r]));
+                    float qx;   // sum q x of the chunk
+                    if constexpr (T::kBytes == 2)
+                        qx = (fmaf(0.0625f, acc[r].y, acc[r].x) * cst.y) * cst.z;
+                    else
+                        qx = acc[r].x + acc[r].y;
+                    part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.x, part[r]));
                 }
             } else {
                 // nothing to read (an iteration past K, or a wait that gave up): release the slot
@@ -367,7 +457,7 @@ bool plan_qmv4(int64_t N, int64_t K, int gs, int tbytes, Qmv4Plan* out) {
     const int sms = num_sms();
     const int n_it = (int)((K + kItCols - 1) / kItCols);
     const int sbg = kItCols / gs;
-    const size_t fixed = (size_t)n_it * (256 + 32) * 16;   // x pieces + chunk constants
+    const size_t fixed = (size_t)n_it * ((tbytes == 4 ? 8 : 4) * 32 * 16 + 32 * 16);   // x pieces + chunk constants
     const size_t cap = 227 * 1024;
     bool found = false;
     int64_t best = 0;
@@ -538,13 +628,6 @@ cudaError_t launch_qmv4(const uint32_t* w, const void* scales, const void* biase
         a.sb_rs = (uint32_t)sbg;
         a.sb_is = p.sb_slice / (uint32_t)tbytes;
     }
-    a.mask_lo = kMaskLo;
-    a.mask_hi = kMaskHi;
-    a.one = kOne;
-    a.k256 = 0x43800000u;    // 256.0f
-    a.k16 = 0x41800000u;     // 16.0f
-    a.km256 = 0xC3800000u;   // -256.0f
-    a.km16 = 0xC1800000u;    // -16.0f
     a.status = status;
     a.spin_limit = spin_limit;
     switch (dtype) {

@@ -182,3 +182,44 @@ def test_width_sweep_full_size_sampled(bits, gs, full_weights):
         assert np.all(np.isfinite(got))
         ref, absdot = oracle.qmm(packed, s, b, x, bits, gs, "bf16", rows=rows)
         assert_within(got[:, rows], ref, absdot, "bf16", f"bits={bits} gs={gs} M={M}")
+
+
+def _x_extremes(K, dtype, seed):
+    """x whose 32-element chunks are: all zero, tiny, huge, spanning many
+    binades, subnormal in the type, and ordinary N(0, 1)."""
+    r = np.random.default_rng(seed)
+    big, small, sub = (1e30, 1e-30, 1e-39) if dtype == "bf16" else (2e4, 1e-4, 3e-7)
+    x = r.standard_normal(K).astype(np.float64)
+    for c in range(K // 32):
+        sl = slice(32 * c, 32 * c + 32)
+        kind = c % 6
+        if kind == 0:
+            x[sl] = 0.0
+        elif kind == 1:
+            x[sl] *= small
+        elif kind == 2:
+            x[sl] *= big / 4
+        elif kind == 3:
+            x[sl] *= np.where(r.random(32) < 0.5, big / 4, small)
+        elif kind == 4:
+            x[sl] = r.choice([-1.0, 1.0], 32) * sub * r.integers(1, 8, 32)
+    return _bits_of(x.astype(np.float32), dtype)
+
+
+def _bits_of(x32, dtype):
+    t = torch.from_numpy(x32).to(TORCH_DTYPE[dtype])
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_qmv_4bit_x_extreme_ranges(dtype, gs):
+    """The 4-bit qmv kernel on x with zero, tiny, huge, wide-range and
+    subnormal chunks (the bf16 path scales each chunk by a power of two)."""
+    N, K = 96, 4096
+    _, packed, s, b, _ = affine_problem(N, K, 1, 4, gs, dtype, seed=gs + 5)
+    x = _x_extremes(K, dtype, gs)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, gs, dtype)
+    got = _run_qmv(packed, s, b, x, 4, gs, dtype)
+    assert np.all(np.isfinite(got))
+    assert_within(got, ref, absdot, dtype, f"qmv x extremes {dtype} gs={gs}")
