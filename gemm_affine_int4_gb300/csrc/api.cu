@@ -128,6 +128,8 @@ static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, i
         // group size, >= 256 columns; K < 512 is never split)
         if (!uniform_plan(N, K, gs, split_k, &p)) return GAI4_ERR_UNSUPPORTED;
         if (split_k > 1 && !tc) return GAI4_ERR_UNSUPPORTED;   // only the tensor-core path splits K
+        // codes other than 4-bit are staged in whole 256-column stages
+        if (split_k > 1 && bits != 4 && (K / split_k) % 256 != 0) return GAI4_ERR_UNSUPPORTED;
     }
     *path = tc ? 1 : 0;
     *plan = p;

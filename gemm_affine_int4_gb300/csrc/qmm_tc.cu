@@ -334,7 +334,8 @@ struct Params {
     int a_stages;
     int n_issuers;        // MMA issuer warps = accumulators (1 or 2)
     int sb_boxes;         // 8-group boxes per stage and tensor reserved in shared memory (1 or 2)
-    uint32_t nib_mask;    // 0x000F000F
+    int mchunk;           // x rows per M chunk (blockIdx.z)
+    uint32_t nib_mask;    // code mask in both halves (0x000F000F for 4-bit codes)
     uint32_t magic;       // bit pattern of C (128 for bf16, 1024 for f16) in both halves
     int* status;
     long long spin_limit;
@@ -389,6 +390,113 @@ __device__ __forceinline__ void dequant_word4(uint32_t w, uint32_t s2, uint32_t 
     o[3] = __byte_perm(r[2], r[3], 0x7632);   // (w6, w7)
 }
 
+template <bool BF>
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (BF)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bits [P, P + 32) of the 96-bit little-endian value (u0, u1, u2), P a
+// compile-time constant below 96
+template <int P>
+__device__ __forceinline__ uint32_t win96(uint32_t u0, uint32_t u1, uint32_t u2) {
+    if constexpr (P == 0) return u0;
+    else if constexpr (P < 32) return __funnelshift_r(u0, u1, P);
+    else if constexpr (P == 32) return u1;
+    else if constexpr (P < 64) return __funnelshift_r(u1, u2, P - 32);
+    else if constexpr (P == 64) return u2;
+    else return u2 >> (P - 64);
+}
+
+// eight w_hat pairs (j, j + H) -> the eight pairs (k, k + 1) of 2H codes
+template <int H>
+__device__ __forceinline__ void pairs_from_halves(const uint32_t* r, uint32_t* o) {
+#pragma unroll
+    for (int i = 0; i < H / 2; ++i) {
+        o[i] = __byte_perm(r[2 * i], r[2 * i + 1], 0x5410);           // codes 2i, 2i + 1
+        o[H / 2 + i] = __byte_perm(r[2 * i], r[2 * i + 1], 0x7632);   // codes H + 2i, H + 2i + 1
+    }
+}
+
+// 2-bit codes: one word (code j at bits 2j) -> 8 pairs (k, k + 1)
+template <bool BF>
+__device__ __forceinline__ void dequant16_b2(uint32_t w, uint32_t s2, uint32_t b2, uint32_t mask, uint32_t magic,
+                                             uint32_t* o) {
+    constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
+    uint32_t r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t p = lop3_andor(w >> (2 * j), mask, magic);   // (C + q_j, C + q_{j+8})
+        r[j] = hfma2<BF>(hsub2<BF>(p, kMagic), s2, b2);
+    }
+    pairs_from_halves<8>(r, o);
+}
+
+// 6-bit codes: 96 bits (code j at bits 6j) -> 8 pairs (k, k + 1)
+template <bool BF, int J = 0>
+__device__ __forceinline__ void b6_pair(uint32_t u0, uint32_t u1, uint32_t u2, uint32_t s2, uint32_t b2,
+                                        uint32_t mask, uint32_t magic, uint32_t* r) {
+    if constexpr (J < 8) {
+        constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
+        // code J at bits 0..5 of the first window, code J + 8 at bits 16..21 of the second
+        const uint32_t a = win96<6 * J>(u0, u1, u2), b = win96<6 * J + 32>(u0, u1, u2);
+        const uint32_t p = lop3_andor(__byte_perm(a, b, 0x7610), mask, magic);
+        r[J] = hfma2<BF>(hsub2<BF>(p, kMagic), s2, b2);
+        b6_pair<BF, J + 1>(u0, u1, u2, s2, b2, mask, magic, r);
+    }
+}
+template <bool BF>
+__device__ __forceinline__ void dequant16_b6(uint32_t u0, uint32_t u1, uint32_t u2, uint32_t s2, uint32_t b2,
+                                             uint32_t mask, uint32_t magic, uint32_t* o) {
+    uint32_t r[8];
+    b6_pair<BF>(u0, u1, u2, s2, b2, mask, magic, r);
+    pairs_from_halves<8>(r, o);
+}
+
+// 3-bit codes: 96 bits (code j at bits 3j) -> 16 pairs (k, k + 1)
+template <bool BF, int J = 0>
+__device__ __forceinline__ void b3_pair(uint32_t u0, uint32_t u1, uint32_t u2, uint32_t s2, uint32_t b2,
+                                        uint32_t mask, uint32_t magic, uint32_t* r) {
+    if constexpr (J < 16) {
+        constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
+        // code J at bits 0..2 of the first window, code J + 16 at bits 16..18 of the second
+        const uint32_t a = win96<3 * J>(u0, u1, u2), b = win96<3 * J + 32>(u0, u1, u2);
+        const uint32_t p = lop3_andor(__byte_perm(a, b, 0x7610), mask, magic);
+        r[J] = hfma2<BF>(hsub2<BF>(p, kMagic), s2, b2);
+        b3_pair<BF, J + 1>(u0, u1, u2, s2, b2, mask, magic, r);
+    }
+}
+template <bool BF>
+__device__ __forceinline__ void dequant32_b3(uint32_t u0, uint32_t u1, uint32_t u2, uint32_t s2, uint32_t b2,
+                                             uint32_t mask, uint32_t magic, uint32_t (&o0)[8], uint32_t (&o1)[8]) {
+    uint32_t r[16];
+    b3_pair<BF>(u0, u1, u2, s2, b2, mask, magic, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o0[i] = __byte_perm(r[2 * i], r[2 * i + 1], 0x5410);   // codes 2i, 2i + 1
+        o1[i] = __byte_perm(r[2 * i], r[2 * i + 1], 0x7632);   // codes 16 + 2i, 17 + 2i
+    }
+}
+
+// 8-bit codes: 4 words (16 codes) -> 8 pairs (k, k + 1). A byte placed in the
+// low bits of a 16-bit half is that byte times the smallest subnormal (the
+// exponent field is 0 or 1); two exact power-of-two products (k1 * k2 =
+// 2^133 for bf16, 2^24 for f16) make it the code.
+template <bool BF>
+__device__ __forceinline__ void dequant16_b8(const uint32_t* u, uint32_t s2, uint32_t b2, uint32_t k1, uint32_t k2,
+                                             uint32_t* o) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t lo = __byte_perm(u[m], 0u, 0x4140), hi = __byte_perm(u[m], 0u, 0x4342);
+        o[2 * m] = hfma2<BF>(hmul2<BF>(hmul2<BF>(lo, k1), k2), s2, b2);
+        o[2 * m + 1] = hfma2<BF>(hmul2<BF>(hmul2<BF>(hi, k1), k2), s2, b2);
+    }
+}
+
 // stage i's groups [g_first, g_last] lie in one or two 8-group TMA boxes
 // starting at group x0 (a multiple of 8: 16-byte aligned box origin)
 __device__ __forceinline__ void stage_groups(int64_t kst, int ncols, int lg, int& x0, int& nbox) {
@@ -398,9 +506,9 @@ __device__ __forceinline__ void stage_groups(int64_t kst, int ncols, int lg, int
     nbox = (g_last - x0) / 8 + 1;
 }
 
-template <bool BF, bool SBT>
+template <int BITS, bool BF, bool SBT>
 __global__ void __launch_bounds__(kThreads, 1)
-    qmm_tc4_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+    qmm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap bmap,
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -412,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mt = p.mt;
     const int XS = p.x_stages, WS = p.w_stages, AS = p.a_stages;
     const uint32_t x_stage_bytes = (uint32_t)mt * kXBK * 2;    // two 64-column swizzle atoms
-    const uint32_t w_stage_bytes = kTileN * kBK / 2;           // 4-bit codes, 128-byte rows
+    const uint32_t w_stage_bytes = kTileN * kBK * BITS / 8;    // 32 * BITS bytes per row (two boxes for 6, 8 bits)
     uint8_t* xbuf = smem;
     uint8_t* wbuf = xbuf + (size_t)XS * x_stage_bytes;
     const uint32_t sb_stage_bytes = 2u * kSbBox * (uint32_t)p.sb_boxes;
@@ -433,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t k_begin, k_end;
     piece_of(p.plan, p.K, blockIdx.x, tile, piece, s_t, k_begin, k_end);
     const int64_t n0 = (int64_t)tile * kTileN;
-    const int64_t m0 = (int64_t)blockIdx.z * kMaxMt;
+    const int64_t m0 = (int64_t)blockIdx.z * p.mchunk;
     const int nk64 = (int)((k_end - k_begin) / 64);            // 64-column units in this piece
     const int nst = (nk64 + 3) / 4;                            // 256-column weight / A stages
     const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
@@ -445,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0) {
         for (int i = 0; i < nst && i < WS; ++i) {
             const int64_t kst = k_begin + (int64_t)kBK * i;
-            tma_prefetch_2d(&wmap, (int)(kst / 8), (int)n0);
+            tma_prefetch_2d(&wmap, (int)(kst * BITS / 32), (int)n0);
+            if constexpr (BITS == 6 || BITS == 8) tma_prefetch_2d(&wmap, (int)(kst * BITS / 32) + 4 * BITS, (int)n0);
             if constexpr (SBT) {
                 int x0 = 0, nbox = 0;
                 stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
@@ -502,8 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int x0 = 0, nbox = 0;
                 if constexpr (SBT) stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
                 mbar_arrive_expect_tx(&w_full[s], w_stage_bytes + 2u * kSbBox * (uint32_t)nbox);
-                // x coordinate in 32-bit words: (k_begin + 256 i) * 4 / 32
-                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst / 8), (int)n0);
+                // x coordinate in 32-bit words: (k_begin + 256 i) * BITS / 32; 6- and
+                // 8-bit stages come as two 128-column boxes
+                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst * BITS / 32), (int)n0);
+                if constexpr (BITS == 6 || BITS == 8)
+                    tma_load_2d(wbuf + (size_t)s * w_stage_bytes + w_stage_bytes / 2, &wmap, &w_full[s],
+                                (int)(kst * BITS / 32) + 4 * BITS, (int)n0);
                 if constexpr (SBT) {
                     uint8_t* sb = sbbuf + (size_t)s * sb_stage_bytes;
                     for (int bx = 0; bx < nbox; ++bx) {
@@ -607,6 +720,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t wc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) wc[c] = wrow_s + 16u * (uint32_t)((4 * hw + c) ^ (r & 7));
+        // other widths: the BITS 16-byte granules of this thread's 128 columns
+        // (2 bits: 64-byte rows, 64-byte swizzle; 3 bits: 96-byte rows; 6 bits:
+        // two boxes of 96-byte rows; 8 bits: two boxes of 128-byte rows,
+        // 128-byte swizzle)
+        uint32_t wg[BITS];
+#pragma unroll
+        for (int c = 0; c < BITS; ++c) {
+            uint32_t lin;
+            if constexpr (BITS == 2) {
+                lin = (uint32_t)r * 64u + (uint32_t)hw * 32u + 16u * c;
+                lin ^= ((lin >> 7) & 3u) << 4;
+            } else if constexpr (BITS == 3) {
+                lin = (uint32_t)r * 96u + (uint32_t)hw * 48u + 16u * c;
+            } else if constexpr (BITS == 6) {
+                lin = (uint32_t)hw * (kTileN * 96u) + (uint32_t)r * 96u + 16u * c;
+            } else {
+                lin = (uint32_t)hw * (kTileN * 128u) + (uint32_t)r * 128u + 16u * c;
+                lin ^= ((lin >> 7) & 7u) << 4;
+            }
+            wg[c] = smem_u32(wbuf) + lin;
+        }
+        // 8-bit codes: the two power-of-two factors that make a subnormal byte the code
+        const uint32_t k1 = pin_reg(BF ? 0x7F007F00u : 0x6C006C00u), k2 = pin_reg(BF ? 0x42804280u : 0x6C006C00u);
         const uint32_t ta0 = tmem_base + lane_base + a_col0;
         // TMA-staged scales / biases: row r of each 8-group box, in slot 0
         const uint32_t sb0 = smem_u32(sbbuf) + (uint32_t)r * 16u;
@@ -655,9 +791,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_sb(i + 4, s1, b1);
             }
             if (!warp_wait(&w_full[sw], (uint32_t)pw, ctl)) break;
-            uint4 v[4];
+            uint4 v[BITS];
+            if constexpr (BITS == 4) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = lds128(wc[c] + w_off);
+                for (int c = 0; c < 4; ++c) v[c] = lds128(wc[c] + w_off);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BITS; ++c) v[c] = lds128(wg[c] + w_off);
+            }
             if constexpr (SBT) {
                 // group of each quarter relative to the slot's first box origin
                 // (g rounded down to a multiple of 8): box (idx >> 3), column
@@ -683,16 +824,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ta = ta0 + (uint32_t)sa * kAStageCols;
             // one 8-column store per word pair (a quarter past the piece is
             // decoded from whatever the slot holds; its columns are not read)
+            uint32_t s2[4], b2[4];   // scale / bias of each 32-column quarter in both halves
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint32_t s2 = __byte_perm(sc[c], 0u, 0x1010), b2 = __byte_perm(bc[c], 0u, 0x1010);
-                uint32_t o8[8];
-                dequant_word4<BF>(v[c].x, s2, b2, nibm, magic, &o8[0]);
-                dequant_word4<BF>(v[c].y, s2, b2, nibm, magic, &o8[4]);
-                tmem_st8(ta + 16u * c, o8);
-                dequant_word4<BF>(v[c].z, s2, b2, nibm, magic, &o8[0]);
-                dequant_word4<BF>(v[c].w, s2, b2, nibm, magic, &o8[4]);
-                tmem_st8(ta + 16u * c + 8u, o8);
+                s2[c] = __byte_perm(sc[c], 0u, 0x1010);
+                b2[c] = __byte_perm(bc[c], 0u, 0x1010);
+            }
+            if constexpr (BITS == 4) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o8[8];
+                    dequant_word4<BF>(v[c].x, s2[c], b2[c], nibm, magic, &o8[0]);
+                    dequant_word4<BF>(v[c].y, s2[c], b2[c], nibm, magic, &o8[4]);
+                    tmem_st8(ta + 16u * c, o8);
+                    dequant_word4<BF>(v[c].z, s2[c], b2[c], nibm, magic, &o8[0]);
+                    dequant_word4<BF>(v[c].w, s2[c], b2[c], nibm, magic, &o8[4]);
+                    tmem_st8(ta + 16u * c + 8u, o8);
+                }
+            } else {
+                const uint32_t* u = reinterpret_cast<const uint32_t*>(v);   // 4 * BITS words, 128 codes
+                if constexpr (BITS == 2) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {   // 16 codes per word
+                        uint32_t o8[8];
+                        dequant16_b2<BF>(u[m], s2[m >> 1], b2[m >> 1], nibm, magic, o8);
+                        tmem_st8(ta + 8u * m, o8);
+                    }
+                } else if constexpr (BITS == 3) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {   // 32 codes per 3 words
+                        uint32_t o0[8], o1[8];
+                        dequant32_b3<BF>(u[3 * m], u[3 * m + 1], u[3 * m + 2], s2[m], b2[m], nibm, magic, o0, o1);
+                        tmem_st8(ta + 16u * m, o0);
+                        tmem_st8(ta + 16u * m + 8u, o1);
+                    }
+                } else if constexpr (BITS == 6) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {   // 16 codes per 3 words
+                        uint32_t o8[8];
+                        dequant16_b6<BF>(u[3 * m], u[3 * m + 1], u[3 * m + 2], s2[m >> 1], b2[m >> 1], nibm, magic,
+                                         o8);
+                        tmem_st8(ta + 8u * m, o8);
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {   // 16 codes per 4 words
+                        uint32_t o8[8];
+                        dequant16_b8<BF>(&u[4 * m], s2[m >> 1], b2[m >> 1], k1, k2, o8);
+                        tmem_st8(ta + 8u * m, o8);
+                    }
+                }
             }
             tmem_st_wait();
             fence_before();
@@ -784,32 +965,126 @@ using tc::kTmemCols;
 int qmm_tc_supported(int64_t M, int64_t N, int64_t K, int bits, int gs) {
     (void)M;
     (void)N;
-    if (bits != 4) return 0;
+    if (bits != 2 && bits != 3 && bits != 4 && bits != 6 && bits != 8) return 0;
     if (K % 64 != 0 || gs < 32) return 0;   // 64-column halves, whole groups
     if (K > (int64_t)1 << 30) return 0;       // column offsets are kept in 32-bit registers
+    // other widths: whole 256-column stages (every piece starts on one) and
+    // packed rows a multiple of 16 bytes (TMA row stride)
+    if (bits != 4 && (K % 256 != 0 || (K * bits / 8) % 16 != 0)) return 0;
     return 1;
+}
+
+// Ring depths for x rows padded to mt and the given code width; false when
+// they do not fit. One CTA per SM: a second co-resident CTA of this kernel
+// could run warps whose tensor-memory lane quadrant differs from
+// (warp index % 4), which the dequantize and epilogue roles rely on; the
+// kernel also takes all 512 tensor-memory columns. The shared-memory request
+// is kept above half of the SM's capacity.
+// Two issuers (two accumulators) while they leave room for four A stages
+// (one per dequantize group). Ring depths and slot ownership: a ring slot
+// must always be waited on by the same role, phase after phase, because
+// mbarrier.try_wait.parity reports a phase two ahead of the barrier as
+// complete. Hence, with two issuers taking alternate stages, the A and
+// activation rings have even depth; the weight ring has even depth (two of
+// the four dequantize groups read the even weight stages, two the odd ones);
+// and the A ring holds at least the four stages of the four groups.
+// The weight ring gets the shared memory first: its stages stream from DRAM
+// and the bytes in flight per SM set the bandwidth; activation tiles are L2
+// hits and need only a short ring (at least 3 stages, 2 for the widest tiles).
+static bool size_rings(int mt, int bits, int sb_boxes, int* ni_out, int* as_out, int* ws_out, int* xs_out,
+                       size_t* smem_out) {
+    const int ni = (tc::kMaxIssuers * mt + 4 * (int)tc::kAStageCols <= kTmemCols) ? tc::kMaxIssuers : 1;
+    int as = (kTmemCols - ni * mt) / (int)tc::kAStageCols;
+    as = as > kMaxAStages ? kMaxAStages : as;
+    if (ni == 2) as &= ~1;
+    if (as < 4) return false;
+    const size_t kBars = 512;
+    const size_t x_stage = (size_t)mt * tc::kXBK * 2;
+    const size_t w_stage = (size_t)kTileN * kBK * bits / 8 + 2u * tc::kSbBox * (size_t)sb_boxes;
+    const size_t budget = 224 * 1024 - 1024 - kBars;
+    const int xs_min = mt > 128 ? 2 : (ni == 2 ? 4 : 3);
+    if ((size_t)xs_min * x_stage + 4 * w_stage > budget) return false;
+    int ws = (int)((budget - (size_t)xs_min * x_stage) / w_stage);
+    ws = ws > kMaxWStages ? kMaxWStages : ws;
+    ws &= ~1;
+    int xs = (int)((budget - (size_t)ws * w_stage) / x_stage);
+    xs = xs > kMaxXStages ? kMaxXStages : xs;
+    if (ni == 2) xs &= ~1;
+    if (ws < 4 || xs < xs_min) return false;
+    size_t smem = 1024 + (size_t)xs * x_stage + (size_t)ws * w_stage + kBars;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    if (smem > 227 * 1024) return false;
+    static_assert((2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxAStages + 1) * 8 + 8 <= 512, "barrier area");
+    *ni_out = ni;
+    *as_out = as;
+    *ws_out = ws;
+    *xs_out = xs;
+    *smem_out = smem;
+    return true;
 }
 
 cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int64_t M = L.M, N = L.N, K = L.K;
-    const int64_t mchunks = (M + kMaxMt - 1) / kMaxMt;
-    const int64_t mrows = M < kMaxMt ? M : kMaxMt;
-    const int mt = (int)((mrows + 15) / 16 * 16);
+    const int bits = L.bits;
+    if (!qmm_tc_supported(M, N, K, bits, L.group_size)) return cudaErrorInvalidValue;
 
-    // packed weights: u32 [N, K/8], box {32 words = 256 columns, 128 rows}, 128-byte swizzle
+    // packed weights: u32 [N, K * bits / 32], one box of 256 columns x 128 rows
+    // per stage (two of 128 columns for 6 and 8 bits): 4 bits 128-byte rows and
+    // 2 bits 64-byte rows, swizzled at their width; 3 and 6 bits 96-byte rows
+    // (16-byte reads of rows 96 bytes apart already spread over the banks);
+    // 8 bits 128-byte rows, 128-byte swizzle
     CUtensorMap wmap, xmap, smap, bmap;
     {
-        cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {32, 128};
+        cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 32), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K * bits / 8)};
+        const cuuint32_t bw = (bits == 6 || bits == 8) ? (cuuint32_t)(4 * bits) : (cuuint32_t)(8 * bits);
+        cuuint32_t box[2] = {bw, 128};
         cuuint32_t es[2] = {1, 1};
+        const CUtensorMapSwizzle sw = bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                      : (bits == 4 || bits == 8) ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                                 : CU_TENSOR_MAP_SWIZZLE_NONE;
         if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(L.w), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // x rows per M chunk: the largest multiple of 16 (at most 256) whose rings
+    // fit in shared memory next to this width's weight stages
+    int mchunk = 0, mt = 0, ni = 0, as = 0, ws = 0, xs = 0, sb_boxes = 0;
+    size_t smem = 0;
+    const int64_t groups = K / L.group_size;
+    const bool sbt = groups % 8 == 0 && (reinterpret_cast<uintptr_t>(L.scales) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(L.biases) & 15u) == 0;
+    // one box of scales / biases per stage suffices when every piece starts on
+    // a 256-column boundary (then so does every stage)
+    if (sbt) {
+        bool aligned = true;
+        const int64_t KU = K / L.plan.unit;
+        for (int st = L.plan.s_base; st <= L.plan.s_base + (L.plan.n_extra > 0 ? 1 : 0); ++st)
+            for (int j = 0; j < st; ++j)
+                if (((j * KU / st) * L.plan.unit) % 256 != 0) aligned = false;
+        sb_boxes = aligned ? 1 : 2;
+    }
+    for (int cap = kMaxMt; cap >= 16 && mchunk == 0; cap -= 16) {
+        const int64_t mrows = M < cap ? M : cap;
+        const int mt_c = (int)((mrows + 15) / 16 * 16);
+        int ni_c, as_c, ws_c, xs_c;
+        size_t smem_c;
+        if (size_rings(mt_c, bits, sb_boxes, &ni_c, &as_c, &ws_c, &xs_c, &smem_c)) {
+            mchunk = cap;
+            mt = mt_c;
+            ni = ni_c;
+            as = as_c;
+            ws = ws_c;
+            xs = xs_c;
+            smem = smem_c;
+        }
+    }
+    if (mchunk == 0) return cudaErrorInvalidValue;
+    const int64_t mchunks = (M + mchunk - 1) / mchunk;
+
     // activations: 16-bit [M, K], box {64 columns, mt rows}, 128-byte swizzle
     {
         cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -826,9 +1101,6 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     // (16-byte rows, no swizzle); the row stride and both base addresses must
     // be multiples of 16 bytes, otherwise the dequantize warps load them from
     // global memory
-    const int64_t groups = K / L.group_size;
-    const bool sbt = groups % 8 == 0 && (reinterpret_cast<uintptr_t>(L.scales) & 15u) == 0 &&
-                     (reinterpret_cast<uintptr_t>(L.biases) & 15u) == 0;
     memset(&smap, 0, sizeof(smap));
     memset(&bmap, 0, sizeof(bmap));
     if (sbt) {
@@ -845,55 +1117,6 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
                 return cudaErrorInvalidValue;
     }
 
-    // Ring depths. One CTA per SM: a second co-resident CTA of this kernel
-    // could run warps whose tensor-memory lane quadrant differs from
-    // (warp index % 4), which the dequantize and epilogue roles rely on; the
-    // kernel also takes all 512 tensor-memory columns. The shared-memory
-    // request is kept above half of the SM's capacity.
-    // Two issuers (two accumulators) while they leave room for four A stages
-    // (one per dequantize group). Ring depths and slot ownership: a ring slot
-    // must always be waited on by the same role, phase after phase, because
-    // mbarrier.try_wait.parity reports a phase two ahead of the barrier as
-    // complete. Hence, with two issuers taking alternate stages, the A and
-    // activation rings have even depth; the weight ring has even depth (two
-    // of the four dequantize groups read the even weight stages, two the odd
-    // ones); and the A ring holds at least the four stages of the four groups.
-    const int ni = (tc::kMaxIssuers * mt + 4 * (int)tc::kAStageCols <= kTmemCols) ? tc::kMaxIssuers : 1;
-    int as = (kTmemCols - ni * mt) / (int)tc::kAStageCols;
-    as = as > kMaxAStages ? kMaxAStages : as;
-    if (ni == 2) as &= ~1;
-    if (as < 4) return cudaErrorInvalidValue;
-    // one box of scales / biases per stage suffices when every piece starts on
-    // a 256-column boundary (then so does every stage)
-    int sb_boxes = 0;
-    if (sbt) {
-        bool aligned = true;
-        const int64_t KU = K / L.plan.unit;
-        for (int st = L.plan.s_base; st <= L.plan.s_base + (L.plan.n_extra > 0 ? 1 : 0); ++st)
-            for (int j = 0; j < st; ++j)
-                if (((j * KU / st) * L.plan.unit) % 256 != 0) aligned = false;
-        sb_boxes = aligned ? 1 : 2;
-    }
-    // The weight ring gets the shared memory first: its stages stream from
-    // DRAM and the bytes in flight per SM set the bandwidth (about 7 stages
-    // of 16 KB are needed); activation tiles are L2 hits and need only a
-    // short ring (at least 3 stages, 2 for the widest tiles).
-    const size_t kBars = 512;
-    const size_t x_stage = (size_t)mt * tc::kXBK * 2;
-    const size_t w_stage = (size_t)kTileN * kBK / 2 + 2u * tc::kSbBox * (size_t)sb_boxes;
-    const size_t budget = 224 * 1024 - 1024 - kBars;
-    const int xs_min = mt > 128 ? 2 : (ni == 2 ? 4 : 3);
-    int ws = (int)((budget - (size_t)xs_min * x_stage) / w_stage);
-    ws = ws < 4 ? 4 : (ws > kMaxWStages ? kMaxWStages : ws);
-    ws &= ~1;
-    int xs = (int)((budget - (size_t)ws * w_stage) / x_stage);
-    xs = xs < 2 ? 2 : (xs > kMaxXStages ? kMaxXStages : xs);
-    if (ni == 2) xs &= ~1;
-    const size_t x_bytes = (size_t)xs * x_stage;
-    size_t smem = 1024 + x_bytes + (size_t)ws * w_stage + kBars;
-    if (smem < 120 * 1024) smem = 120 * 1024;
-    static_assert((2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxAStages + 1) * 8 + 8 <= 512, "barrier area");
-
     tc::Params p;
     p.scales = static_cast<const uint16_t*>(L.scales);
     p.biases = static_cast<const uint16_t*>(L.biases);
@@ -908,24 +1131,30 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.gs_log2 = lg;
     p.plan = L.plan;
     p.mt = mt;
+    p.mchunk = mchunk;
     p.x_stages = xs;
     p.w_stages = ws;
     p.a_stages = as;
     if ((ni == 2 && ((xs | as) & 1)) || (ws & 1) || ws < 4) return cudaErrorInvalidValue;   // ring invariants above
     p.n_issuers = ni;
     p.sb_boxes = sb_boxes > 0 ? sb_boxes : 1;
-    p.nib_mask = 0x000F000Fu;
+    p.nib_mask = bits == 2 ? 0x00030003u : bits == 3 ? 0x00070007u : bits == 6 ? 0x003F003Fu : 0x000F000Fu;
     p.magic = L.is_bf16 ? 0x43004300u : 0x64006400u;
     p.status = L.status;
     p.spin_limit = L.spin_limit;
 
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                             const tc::Params);
-    static const KernFn kernels[4] = {tc::qmm_tc4_kernel<false, false>, tc::qmm_tc4_kernel<true, false>,
-                                      tc::qmm_tc4_kernel<false, true>, tc::qmm_tc4_kernel<true, true>};
-    const int which = (L.is_bf16 ? 1 : 0) + (sbt ? 2 : 0);
+#define GAI4_TC_KERNELS(B)                                                                                  \
+    tc::qmm_tc_kernel<B, false, false>, tc::qmm_tc_kernel<B, true, false>, tc::qmm_tc_kernel<B, false, true>, \
+        tc::qmm_tc_kernel<B, true, true>
+    static const KernFn kernels[20] = {GAI4_TC_KERNELS(2), GAI4_TC_KERNELS(3), GAI4_TC_KERNELS(4), GAI4_TC_KERNELS(6),
+                                       GAI4_TC_KERNELS(8)};
+#undef GAI4_TC_KERNELS
+    const int wi = bits == 2 ? 0 : bits == 3 ? 1 : bits == 4 ? 2 : bits == 6 ? 3 : 4;
+    const int which = 4 * wi + (L.is_bf16 ? 1 : 0) + (sbt ? 2 : 0);
     const KernFn kern = kernels[which];
-    static unsigned long long configured[4] = {0ull, 0ull, 0ull, 0ull};
+    static unsigned long long configured[20] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !(configured[which] & (1ull << dev))) {

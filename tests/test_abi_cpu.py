@@ -91,6 +91,13 @@ def test_split_rules(lib):
         plan(40, 4096, 640, 4, 64, bf, split_k=4, workspace_bytes=1 << 30)   # 160-long ranges
     with pytest.raises(g4.Gai4Error):
         plan(40, 4096, 5 * 64 * 3, 4, 64, bf, split_k=2, workspace_bytes=1 << 30)  # 480: not a multiple of 128
+    # other code widths take the tensor-core path in whole 256-column stages
+    assert plan(64, 4096, 4096, 6, 64, bf)[0] == 1
+    assert plan(64, 4096, 4096 + 64, 3, 64, bf)[0] == 0
+    assert plan(33, 4096, 3072, 8, 64, bf, split_k=3, workspace_bytes=1 << 30) == (1, 3)
+    assert plan(33, 4096, 2560, 2, 64, bf, split_k=2, workspace_bytes=1 << 30) == (1, 2)
+    with pytest.raises(g4.Gai4Error):
+        plan(33, 4096, 2560, 2, 64, bf, split_k=4, workspace_bytes=1 << 30)   # 640-column pieces
     # f32 never takes the tensor-core path and never splits
     assert plan(64, 4096, 4096, 4, 64, torch.float32) == (0, 1)
     # no workspace, automatic: no split

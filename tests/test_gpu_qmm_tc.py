@@ -140,3 +140,44 @@ def test_tc_misaligned_scales_biases(offset):
         assert g4.gai4_last_device_status() == 0
         assert torch.equal(out_a, out_m)
         assert_within(to_host_f64(out_m, "bf16"), ref, absdot, "bf16", f"misaligned scales S={S}")
+
+
+# tensor-core path for 2-, 3-, 6- and 8-bit codes (whole 256-column stages):
+# ragged tiles, several M chunks (the wider codes take smaller chunks), every
+# legal split
+WIDTH_CASES = [(131, 1024, 9), (256, 2048, 40), (300, 1536, 100), (129, 4096, 300)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bits,gs", [(2, 32), (3, 64), (6, 128), (8, 64)])
+@pytest.mark.parametrize("N,K,M", WIDTH_CASES)
+def test_tc_other_widths(N, K, M, bits, gs, dtype):
+    _, packed, s, b, x = affine_problem(N, K, M, bits, gs, dtype, seed=N + K + M + bits)
+    assert g4.gai4_qmm_t_plan(M, N, K, bits, gs, TORCH_DTYPE[dtype])[0] == 1
+    ref, absdot = oracle.qmm(packed, s, b, x, bits, gs, dtype)
+    for S in (1, 2, 3, 4):
+        try:
+            g4.gai4_qmm_t_plan(M, N, K, bits, gs, TORCH_DTYPE[dtype], split_k=S, workspace_bytes=1 << 40)
+        except g4.Gai4Error:
+            continue
+        out = _run(packed, s, b, x, dtype, split_k=S, bits=bits, gs=gs)
+        assert_within(to_host_f64(out, dtype), ref, absdot, dtype, f"tc {bits}-bit N={N} K={K} M={M} S={S} {dtype}")
+
+
+def test_tc_8bit_every_code():
+    """Every 8-bit code value, including those at and above 128 (whose 16-bit
+    pattern has the exponent field 1 instead of 0), in every row."""
+    N, K, M, gs = 128, 1024, 16, 64
+    r = np.random.default_rng(3)
+    q = np.tile(np.arange(256, dtype=np.uint32), (N, K // 256))
+    q = np.stack([np.roll(q[i], 7 * i) for i in range(N)])
+    packed = oracle.pack(q, 8)
+    sc = r.uniform(1e-3, 1e-2, (N, K // gs)).astype(np.float32)
+    bi = r.uniform(-0.5, 0.5, (N, K // gs)).astype(np.float32)
+    sb = torch.from_numpy(sc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bb = torch.from_numpy(bi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    ref, absdot = oracle.qmm(packed, sb, bb, xb, 8, gs, "bf16")
+    out = _run(packed, sb, bb, xb, "bf16", bits=8, gs=gs)
+    assert_within(to_host_f64(out, "bf16"), ref, absdot, "bf16", "tc 8-bit every code")
