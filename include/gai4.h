@@ -122,12 +122,15 @@ gai4_status gai4_qmv(const uint32_t* w_packed, const void* scales, const void* b
  * unsplit, fp32 partials summed by a separate kernel, one rounding after the
  * sum): split_k = 0 lets the library choose; 1..4 forces that split, which
  * must give K ranges that are multiples of 64 and of group_size and at least
- * 256 long (GAI4_ERR_UNSUPPORTED otherwise). With split S > 1 the fp32
+ * 256 long (and, for codes other than 4-bit, multiples of 256;
+ * GAI4_ERR_UNSUPPORTED otherwise). With split S > 1 the fp32
  * partials [S, M, N] live in `workspace` (device, 16-byte aligned,
  * workspace_bytes >= gai4_qmm_t_workspace_bytes(...) for that split). In
  * automatic mode the split is also limited to what `workspace_bytes` holds
  * (workspace may be NULL: no split). The summation order is fixed, so a
  * given split gives bit-identical results run to run.
+ * The tensor-core path takes 2-, 3-, 4-, 6- and 8-bit codes (other widths
+ * than 4 when K is a multiple of 256); everything else runs on CUDA cores.
  * On the tensor-core path scales and biases are fetched by TMA with the
  * packed weights when K / group_size is a multiple of 8 and both base
  * pointers are 16-byte aligned, and read from global memory by the

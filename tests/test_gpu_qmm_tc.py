@@ -181,3 +181,27 @@ def test_tc_8bit_every_code():
     ref, absdot = oracle.qmm(packed, sb, bb, xb, 8, gs, "bf16")
     out = _run(packed, sb, bb, xb, "bf16", bits=8, gs=gs)
     assert_within(to_host_f64(out, "bf16"), ref, absdot, "bf16", "tc 8-bit every code")
+
+
+def test_tc_split_workspace_contents_do_not_matter():
+    """The split-K partials live in the caller's workspace: any leftover
+    bytes there (all ones, random, a previous call's partials) give the same
+    output bits."""
+    N, K, M = 384, 4096, 33
+    _, packed, s, b, x = affine_problem(N, K, M, 4, 64, "bf16", seed=91)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, 64, "bf16")
+    wd, sd, bd, xd = to_dev(packed), to_dev(s, "bf16"), to_dev(b, "bf16"), to_dev(x, "bf16")
+    nbytes = g4.gai4_qmm_t_workspace_bytes(M, N, K, 4, 64, torch.bfloat16, 4)
+    ws = torch.zeros(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    outs = []
+    for fill in ("zero", "ones", "random", "reuse", "reuse"):
+        if fill == "ones":
+            ws.view(torch.int32).fill_(-1)
+        elif fill == "random":
+            ws.view(torch.int32).random_()
+        out = g4.gai4_qmm_t(wd, sd, bd, xd, bits=4, group_size=64, split_k=4, workspace=ws)
+        assert g4.gai4_last_device_status() == 0
+        outs.append(out)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert_within(to_host_f64(outs[0], "bf16"), ref, absdot, "bf16", "split workspace contents")
