@@ -332,6 +332,14 @@ def build_workload(torch, g4, dev, seed=0, only=None):
     GPU (4-bit, gs 64, bf16 scales/biases), x ~ N(0, 1) bf16, Q8_0 / Q4_K
     blocks from the shared seeded generators."""
     import synth
+    # profiling runs of the calls measured beside the step: --only
+    # prefill|gguf|q8_0_i8|batched|sweep[:INDEX]
+    extra = {"prefill": build_prefill, "gguf": build_gguf, "q8_0_i8": build_q8_i8, "batched": build_batched,
+             "sweep": build_sweep}
+    if only and only.partition(":")[0] in extra:
+        fam, _, idx = only.partition(":")
+        cs = extra[fam](torch, g4, dev)
+        return {fam: cs if idx == "" else [cs[int(idx)]]}
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
     bf = torch.bfloat16
@@ -593,8 +601,8 @@ def run_gpu(args, rank, world, local_rank):
                             "frac_of_hbm": round(fam_bytes[fam] / (fam_ms[fam] * 1e-3) / 1e9 / hbm, 3),
                             "bytes": fam_bytes[fam]} for fam in fams},
         "roofline": {"kernel": {"qmv": "qmv4_kernel (qmv, M=1)",
-                                "qmm_t": "qmm_t family (qmm_tc4_kernel + splitk_reduce)",
-                                "q8_0": "q8_0_tma_kernel", "q4_k": "q4_k_tma_kernel"}[dom],
+                                "qmm_t": "qmm_t family (qmm_tc_kernel + splitk_reduce)",
+                                "q8_0": "q8_0_tma_kernel", "q4_k": "q4_k_tma_kernel"}.get(dom, dom),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "launches_per_step": n_launch,
