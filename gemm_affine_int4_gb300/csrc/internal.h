@@ -42,6 +42,7 @@ struct SplitPlan {
     int s_base;
     int n_extra;
     int unit;        // K granularity of the cuts: max(64, group_size)
+    int mcap = 256;  // most x rows per M chunk of the tensor-core kernel
     __host__ __device__ int slots() const { return s_base + (n_extra > 0 ? 1 : 0); }
     __host__ __device__ int64_t pieces() const { return (int64_t)n_extra * (s_base + 1) + (int64_t)(tiles - n_extra) * s_base; }
 };

@@ -203,6 +203,15 @@ SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
             p.n_extra = ne;
         }
     }
+    // Large M: when 128-row M chunks fill at most one wave unsplit, they beat
+    // 256-row chunks whose K splits write M x N fp32 partials per piece and
+    // need the reduce (measured at 4096^2, M = 512: 19.2 against 22.3 us). With
+    // more than one wave the larger chunks' fewer MMA instructions win.
+    if (M > 256 && T * ((M + 127) / 128) <= num_sms()) {
+        p.s_base = 1;
+        p.n_extra = 0;
+        p.mcap = 128;
+    }
     return p;
 }
 
@@ -1067,7 +1076,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
                 if (((j * KU / st) * L.plan.unit) % 256 != 0) aligned = false;
         sb_boxes = aligned ? 1 : 2;
     }
-    for (int cap = kMaxMt; cap >= 16 && mchunk == 0; cap -= 16) {
+    for (int cap = std::min(L.plan.mcap, kMaxMt); cap >= 16 && mchunk == 0; cap -= 16) {
         const int64_t mrows = M < cap ? M : cap;
         const int mt_c = (int)((mrows + 15) / 16 * 16);
         int ni_c, as_c, ws_c, xs_c;
