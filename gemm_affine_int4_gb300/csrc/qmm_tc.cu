@@ -506,6 +506,24 @@ __device__ __forceinline__ void dequant16_b8(const uint32_t* u, uint32_t s2, uin
     }
 }
 
+// bf16, 4-bit codes, scale s with exponent field 1..121: the codes masked
+// straight into bf16 subnormals, (q_j, q_{j+4}) * 2^-133 (bits 0..3 of the
+// halves) or (q_j, q_{j+4}) * 2^-129 (bits 4..7), times s * 2^133 resp.
+// s * 2^129 (exact, exponent-field adds) plus b: the fma sees the same exact
+// s * q + b as the offset form and rounds it the same way. 1 shift, 4 ANDs,
+// 4 fmas and 4 permutes per word.
+__device__ __forceinline__ void dequant_word4_sub(uint32_t w, uint32_t s133, uint32_t s129, uint32_t b2, uint32_t* o) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t r0 = hfma2<true>(w & 0x000F000Fu, s133, b2);    // (w0, w4)
+    const uint32_t r1 = hfma2<true>(w & 0x00F000F0u, s129, b2);    // (w1, w5)
+    const uint32_t r2 = hfma2<true>(w8 & 0x000F000Fu, s133, b2);   // (w2, w6)
+    const uint32_t r3 = hfma2<true>(w8 & 0x00F000F0u, s129, b2);   // (w3, w7)
+    o[0] = __byte_perm(r0, r1, 0x5410);
+    o[1] = __byte_perm(r2, r3, 0x5410);
+    o[2] = __byte_perm(r0, r1, 0x7632);
+    o[3] = __byte_perm(r2, r3, 0x7632);
+}
+
 // stage i's groups [g_first, g_last] lie in one or two 8-group TMA boxes
 // starting at group x0 (a multiple of 8: 16-byte aligned box origin)
 __device__ __forceinline__ void stage_groups(int64_t kst, int ncols, int lg, int& x0, int& nbox) {
@@ -842,13 +860,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (BITS == 4) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t o8[8];
-                    dequant_word4<BF>(v[c].x, s2[c], b2[c], nibm, magic, &o8[0]);
-                    dequant_word4<BF>(v[c].y, s2[c], b2[c], nibm, magic, &o8[4]);
+                    // the subnormal form when s * 2^133 is a finite bf16 (this
+                    // row's scale: lanes may differ; the stores below run converged)
+                    uint32_t o8[8], o8b[8];
+                    const uint32_t e = (sc[c] >> 7) & 0xFFu;
+                    if (BF && e >= 1u && e <= 121u) {
+                        const uint32_t s133 = s2[c] + 0x42804280u, s129 = s2[c] + 0x40804080u;
+                        dequant_word4_sub(v[c].x, s133, s129, b2[c], &o8[0]);
+                        dequant_word4_sub(v[c].y, s133, s129, b2[c], &o8[4]);
+                        dequant_word4_sub(v[c].z, s133, s129, b2[c], &o8b[0]);
+                        dequant_word4_sub(v[c].w, s133, s129, b2[c], &o8b[4]);
+                    } else {
+                        dequant_word4<BF>(v[c].x, s2[c], b2[c], nibm, magic, &o8[0]);
+                        dequant_word4<BF>(v[c].y, s2[c], b2[c], nibm, magic, &o8[4]);
+                        dequant_word4<BF>(v[c].z, s2[c], b2[c], nibm, magic, &o8b[0]);
+                        dequant_word4<BF>(v[c].w, s2[c], b2[c], nibm, magic, &o8b[4]);
+                    }
+                    __syncwarp();
                     tmem_st8(ta + 16u * c, o8);
-                    dequant_word4<BF>(v[c].z, s2[c], b2[c], nibm, magic, &o8[0]);
-                    dequant_word4<BF>(v[c].w, s2[c], b2[c], nibm, magic, &o8[4]);
-                    tmem_st8(ta + 16u * c + 8u, o8);
+                    tmem_st8(ta + 16u * c + 8u, o8b);
                 }
             } else {
                 const uint32_t* u = reinterpret_cast<const uint32_t*>(v);   // 4 * BITS words, 128 codes

@@ -205,3 +205,22 @@ def test_tc_split_workspace_contents_do_not_matter():
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
     assert_within(to_host_f64(outs[0], "bf16"), ref, absdot, "bf16", "split workspace contents")
+
+
+def test_tc_bf16_scales_on_both_decode_forms():
+    """bf16 4-bit tiles decode codes as subnormals when s * 2^133 is a finite
+    bf16 (exponent field 1..121) and by the offset form otherwise; rows of one
+    warp take either form: small, large (>= 2^-5), zero and subnormal scales,
+    interleaved row by row."""
+    N, K, M, gs = 256, 2048, 24, 64
+    _, packed, s, b, x = affine_problem(N, K, M, 4, gs, "bf16", seed=123)
+    s32 = oracle.to_f64(s, "bf16").astype(np.float32)
+    kinds = np.arange(N) % 4
+    s32[kinds == 1] *= 64.0                      # >= 2^-5: the offset form
+    s32[kinds == 2] = 0.0
+    s32[kinds == 3] = np.float32(3.0e-39)         # a bf16 subnormal
+    s = torch.from_numpy(s32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref, absdot = oracle.qmm(packed, s, b, x, 4, gs, "bf16")
+    for S in (1, 2):
+        out = _run(packed, s, b, x, "bf16", split_k=S)
+        assert_within(to_host_f64(out, "bf16"), ref, absdot, "bf16", f"tc scale forms S={S}")
