@@ -108,7 +108,7 @@ static cudaError_t run_qmv(const uint32_t* w, const void* sc, const void* bi, co
 static const int64_t kTcMinM = 3;   // tensor-core path from this many x rows up (bf16/f16; measured crossover)
 
 static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, int dtype, int split_k,
-                            size_t ws_bytes, bool unlimited_ws, int* path, SplitPlan* plan) {
+                            size_t ws_bytes, bool unlimited_ws, int* path, SplitPlan* plan, int64_t batch = 1) {
     gai4_status st = check_affine_shape(dtype, bits, gs, N, K);
     if (st != GAI4_OK) return st;
     if (M <= 0) return GAI4_ERR_INVALID_ARG;
@@ -117,9 +117,9 @@ static gai4_status plan_qmm(int64_t M, int64_t N, int64_t K, int bits, int gs, i
     SplitPlan p;
     if (split_k == 0) {
         if (tc) {
-            const size_t per_slot = (size_t)M * (size_t)N * sizeof(float);
+            const size_t per_slot = (size_t)batch * (size_t)M * (size_t)N * sizeof(float);
             const int max_slots = unlimited_ws ? 4 : (int)std::min<size_t>(4, ws_bytes / per_slot);
-            p = auto_plan(M, N, K, gs, max_slots);
+            p = auto_plan(M, N, K, gs, max_slots, batch);
         } else {
             uniform_plan(N, K, gs, 1, &p);
         }
@@ -362,9 +362,15 @@ static int dtype_bytes(gai4_dtype d) { return d == GAI4_F32 ? 4 : 2; }
 
 extern "C" size_t gai4_qmm_t_batched_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K, int bits,
                                                      int group_size, gai4_dtype dtype, int split_k) {
+    using namespace gai4;
     if (batch < 1 || M < 1 || K < 1) return 0;
-    return gai4::round256((size_t)batch * (size_t)M * (size_t)K * (size_t)gai4::dtype_bytes(dtype)) +
-           gai4_qmm_t_workspace_bytes(M, N, K, bits, group_size, dtype, split_k);
+    const size_t gather = round256((size_t)batch * (size_t)M * (size_t)K * (size_t)dtype_bytes(dtype));
+    int path = 0;
+    SplitPlan plan;
+    if (plan_qmm(M, N, K, bits, group_size, dtype, split_k, 0, true, &path, &plan, batch) != GAI4_OK) return 0;
+    if (path == 1)   // one tensor-core launch over all batches: partials [S, batch * M, N]
+        return gather + (plan.slots() > 1 ? (size_t)plan.slots() * (size_t)batch * (size_t)M * (size_t)N * 4 : 0);
+    return gather + gai4_qmm_t_workspace_bytes(M, N, K, bits, group_size, dtype, split_k);
 }
 
 extern "C" gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* scales, const void* biases,
@@ -401,6 +407,46 @@ extern "C" gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* 
         xbs = M * K;
         ws += need;
         ws_left -= need;
+    }
+    // tensor-core path: one launch over all batches (grid y = batch), the
+    // activations viewed as [batch * M, K] and the output as [batch * M, N]
+    {
+        int path = 0;
+        SplitPlan plan;
+        const gai4_status pst = plan_qmm(M, N, K, bits, group_size, dtype, split_k, ws_left, false, &path, &plan, batch);
+        if (pst != GAI4_OK) return pst;
+        if (path == 1 && xbs == M * K && batch <= 65535) {
+            const int splits = plan.slots();
+            if (splits > 1) {
+                if (!ws_left || ws_left < (size_t)splits * (size_t)batch * (size_t)M * (size_t)N * 4)
+                    return GAI4_ERR_WORKSPACE;
+                if (((uintptr_t)ws & 15u) != 0) return GAI4_ERR_MISALIGNED;
+            }
+            if (((uintptr_t)w_packed & 15u) != 0 || ((uintptr_t)xb & 15u) != 0) return GAI4_ERR_MISALIGNED;
+            QmmTcLaunch T;
+            T.w = w_packed;
+            T.scales = scales;
+            T.biases = biases;
+            T.x = xb;
+            T.out = out;
+            T.partials = splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+            T.M = M;
+            T.N = N;
+            T.K = K;
+            T.batch = batch;
+            T.w_batched = w_batched ? 1 : 0;
+            T.bits = bits;
+            T.group_size = group_size;
+            T.plan = plan;
+            T.is_bf16 = dtype == GAI4_BF16;
+            T.status = status_ptr();
+            T.spin_limit = 2000000000LL;
+            if (!T.status) return GAI4_ERR_CUDA;
+            cudaError_t e = launch_qmm_tc(T, s);
+            if (e != cudaSuccess) return GAI4_ERR_CUDA;
+            if (splits > 1) e = launch_splitk_reduce(T.partials, out, batch * M, N, plan, dtype, s);
+            return from_cuda(e);
+        }
     }
     for (int64_t b = 0; b < batch; ++b) {
         const int64_t e = w_batched ? b : 0;

@@ -51,7 +51,7 @@ int max_pieces(int64_t K, int unit);
 // uniform split S (1..4) if legal
 bool uniform_plan(int64_t N, int64_t K, int gs, int S, SplitPlan* out);
 // balanced automatic plan for the device's SM count, limited to max_slots partial slots
-SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots);
+SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots, int64_t batch = 1);
 
 // tensor-core qmm_t (qmm_tc.cu)
 struct QmmTcLaunch {
@@ -60,8 +60,10 @@ struct QmmTcLaunch {
     const void* biases;
     const void* x;      // [M, K] bf16/f16
     void* out;          // [M, N]
-    float* partials;    // [slots, M, N] fp32 when plan.slots() > 1
-    int64_t M, N, K;
+    float* partials;    // [slots, batch * M, N] fp32 when plan.slots() > 1
+    int64_t M, N, K;    // per batch
+    int64_t batch = 1;  // problems in one launch: x [batch * M, K], out [batch * M, N]
+    int w_batched = 0;  // weights / scales / biases stacked [batch * N, ...] (else shared)
     int bits, group_size;
     SplitPlan plan;
     int is_bf16;

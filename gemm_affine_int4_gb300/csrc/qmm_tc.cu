@@ -167,7 +167,7 @@ bool uniform_plan(int64_t N, int64_t K, int gs, int S, SplitPlan* out) {
     return true;
 }
 
-SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
+SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots, int64_t batch) {
     SplitPlan p;
     p.tiles = (int)((N + 127) / 128);
     // 256-column cuts when K allows: every stage of the tensor-core kernel then
@@ -178,7 +178,7 @@ SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
     p.n_extra = 0;
     const int cap = std::min(max_pieces(K, p.unit), std::max(1, max_slots));
     const int64_t mchunks = (M + 255) / 256;
-    const int64_t avail = std::max<int64_t>(1, num_sms() / mchunks);   // CTAs per M chunk in one wave
+    const int64_t avail = std::max<int64_t>(1, num_sms() / (mchunks * batch));   // CTAs per M chunk and batch in one wave
     const int64_t KU = K / p.unit;
     const int64_t T = p.tiles;
     // candidate 1: uniform S in waves
@@ -207,7 +207,7 @@ SplitPlan auto_plan(int64_t M, int64_t N, int64_t K, int gs, int max_slots) {
     // 256-row chunks whose K splits write M x N fp32 partials per piece and
     // need the reduce (measured at 4096^2, M = 512: 19.2 against 22.3 us). With
     // more than one wave the larger chunks' fewer MMA instructions win.
-    if (M > 256 && T * ((M + 127) / 128) <= num_sms()) {
+    if (M > 256 && T * ((M + 127) / 128) * batch <= num_sms()) {
         p.s_base = 1;
         p.n_extra = 0;
         p.mcap = 128;
@@ -344,6 +344,7 @@ struct Params {
     int n_issuers;        // MMA issuer warps = accumulators (1 or 2)
     int sb_boxes;         // 8-group boxes per stage and tensor reserved in shared memory (1 or 2)
     int mchunk;           // x rows per M chunk (blockIdx.z)
+    int64_t w_rows_b;     // weight / scale rows between batches (N stacked, 0 shared); batch = blockIdx.y
     uint32_t nib_mask;    // code mask in both halves (0x000F000F for 4-bit codes)
     uint32_t magic;       // bit pattern of C (128 for bf16, 1024 for f16) in both halves
     int* status;
@@ -567,8 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tile, piece, s_t;
     int64_t k_begin, k_end;
     piece_of(p.plan, p.K, blockIdx.x, tile, piece, s_t, k_begin, k_end);
-    const int64_t n0 = (int64_t)tile * kTileN;
-    const int64_t m0 = (int64_t)blockIdx.z * p.mchunk;
+    const int64_t n0 = (int64_t)tile * kTileN;                 // first weight row of the tile within its batch
+    const int64_t m0 = (int64_t)blockIdx.z * p.mchunk;         // first x row of the chunk within its batch
+    const int64_t nw0 = (int64_t)blockIdx.y * p.w_rows_b + n0;   // the tile's first row in the weight / scale tensors
+    const int64_t mb0 = (int64_t)blockIdx.y * p.M;              // the batch's first row of x / out
     const int nk64 = (int)((k_end - k_begin) / 64);            // 64-column units in this piece
     const int nst = (nk64 + 3) / 4;                            // 256-column weight / A stages
     const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
@@ -580,14 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0) {
         for (int i = 0; i < nst && i < WS; ++i) {
             const int64_t kst = k_begin + (int64_t)kBK * i;
-            tma_prefetch_2d(&wmap, (int)(kst * BITS / 32), (int)n0);
-            if constexpr (BITS == 6 || BITS == 8) tma_prefetch_2d(&wmap, (int)(kst * BITS / 32) + 4 * BITS, (int)n0);
+            tma_prefetch_2d(&wmap, (int)(kst * BITS / 32), (int)nw0);
+            if constexpr (BITS == 6 || BITS == 8) tma_prefetch_2d(&wmap, (int)(kst * BITS / 32) + 4 * BITS, (int)nw0);
             if constexpr (SBT) {
                 int x0 = 0, nbox = 0;
                 stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
                 for (int bx = 0; bx < nbox; ++bx) {
-                    tma_prefetch_2d(&smap, x0 + 8 * bx, (int)n0);
-                    tma_prefetch_2d(&bmap, x0 + 8 * bx, (int)n0);
+                    tma_prefetch_2d(&smap, x0 + 8 * bx, (int)nw0);
+                    tma_prefetch_2d(&bmap, x0 + 8 * bx, (int)nw0);
                 }
             }
         }
@@ -640,16 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&w_full[s], w_stage_bytes + 2u * kSbBox * (uint32_t)nbox);
                 // x coordinate in 32-bit words: (k_begin + 256 i) * BITS / 32; 6- and
                 // 8-bit stages come as two 128-column boxes
-                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst * BITS / 32), (int)n0);
+                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst * BITS / 32), (int)nw0);
                 if constexpr (BITS == 6 || BITS == 8)
                     tma_load_2d(wbuf + (size_t)s * w_stage_bytes + w_stage_bytes / 2, &wmap, &w_full[s],
-                                (int)(kst * BITS / 32) + 4 * BITS, (int)n0);
+                                (int)(kst * BITS / 32) + 4 * BITS, (int)nw0);
                 if constexpr (SBT) {
                     uint8_t* sb = sbbuf + (size_t)s * sb_stage_bytes;
                     for (int bx = 0; bx < nbox; ++bx) {
-                        tma_load_2d(sb + bx * kSbBox, &smap, &w_full[s], x0 + 8 * bx, (int)n0);
+                        tma_load_2d(sb + bx * kSbBox, &smap, &w_full[s], x0 + 8 * bx, (int)nw0);
                         tma_load_2d(sb + (uint32_t)p.sb_boxes * kSbBox + bx * kSbBox, &bmap, &w_full[s], x0 + 8 * bx,
-                                    (int)n0);
+                                    (int)nw0);
                     }
                 }
                 ++issued;
@@ -668,8 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&x_full[s], x_stage_bytes);
                 uint8_t* dst = xbuf + (size_t)s * x_stage_bytes;
                 const int kx = (int)(k_begin + kXBK * j);
-                tma_load_2d(dst, &xmap, &x_full[s], kx, (int)m0);
-                tma_load_2d(dst + (size_t)mt * 128, &xmap, &x_full[s], kx + 64, (int)m0);
+                tma_load_2d(dst, &xmap, &x_full[s], kx, (int)(mb0 + m0));
+                tma_load_2d(dst + (size_t)mt * 128, &xmap, &x_full[s], kx + 64, (int)(mb0 + m0));
                 ++issued;
             }
             for (int j = (issued > XS ? issued - XS : 0); j < issued; ++j)
@@ -783,8 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gstep2 = 2 * (kBK >> lg);
         int g = (int)(k_begin >> lg) + (grp >> 1) * (kBK >> lg);   // first group of weight stage i / 2
 
-        const uint16_t* srow = p.scales + (row_ok ? row : 0) * p.groups;
-        const uint16_t* brow = p.biases + (row_ok ? row : 0) * p.groups;
+        const uint16_t* srow = p.scales + (row_ok ? (int64_t)blockIdx.y * p.w_rows_b + row : 0) * p.groups;
+        const uint16_t* brow = p.biases + (row_ok ? (int64_t)blockIdx.y * p.w_rows_b + row : 0) * p.groups;
         // scale / bias of the four quarters of A stage i, from global memory
         // (when they do not come by TMA), one of this group's stages ahead
         auto load_sb = [&](int i, uint32_t (&sv)[4], uint32_t (&bv)[4]) {
@@ -942,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             const int64_t mrows = min((int64_t)mt, p.M - m0);
             const bool split = p.plan.slots() > 1;
-            float* pslot = p.partials + (int64_t)piece * p.M * p.N;
+            float* pslot = p.partials + (int64_t)piece * gridDim.y * p.M * p.N;   // slots of [batch * M, N]
             const int nacc = nxs < NI ? nxs : NI;   // accumulators that received MMAs
             for (int c = 8 * grp; c < mt; c += 32) {
                 uint32_t v[8];
@@ -962,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int64_t m = c + j;
                         if (m < mrows) {
                             const float f = __uint_as_float(v[j]);
-                            const int64_t idx = (m0 + m) * p.N + row;
+                            const int64_t idx = (mb0 + m0 + m) * p.N + row;
                             if (split) {
                                 pslot[idx] = f;
                             } else if (BF) {
@@ -1066,6 +1069,8 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int64_t M = L.M, N = L.N, K = L.K;
+    const int64_t B = L.batch > 0 ? L.batch : 1;
+    const int64_t NW = L.w_batched ? B * N : N;   // weight / scale rows in the tensors
     const int bits = L.bits;
     if (!qmm_tc_supported(M, N, K, bits, L.group_size)) return cudaErrorInvalidValue;
 
@@ -1076,7 +1081,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     // 8 bits 128-byte rows, 128-byte swizzle
     CUtensorMap wmap, xmap, smap, bmap;
     {
-        cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 32), (cuuint64_t)N};
+        cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 32), (cuuint64_t)NW};
         cuuint64_t strides[1] = {(cuuint64_t)(K * bits / 8)};
         const cuuint32_t bw = (bits == 6 || bits == 8) ? (cuuint32_t)(4 * bits) : (cuuint32_t)(8 * bits);
         cuuint32_t box[2] = {bw, 128};
@@ -1126,7 +1131,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
 
     // activations: 16-bit [M, K], box {64 columns, mt rows}, 128-byte swizzle
     {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(B * M)};
         cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
         cuuint32_t box[2] = {64, (cuuint32_t)mt};
         cuuint32_t es[2] = {1, 1};
@@ -1143,7 +1148,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     memset(&smap, 0, sizeof(smap));
     memset(&bmap, 0, sizeof(bmap));
     if (sbt) {
-        cuuint64_t dims[2] = {(cuuint64_t)groups, (cuuint64_t)N};
+        cuuint64_t dims[2] = {(cuuint64_t)groups, (cuuint64_t)NW};
         cuuint64_t strides[1] = {(cuuint64_t)(groups * 2)};
         cuuint32_t box[2] = {8, 128};
         cuuint32_t es[2] = {1, 1};
@@ -1162,6 +1167,7 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
     p.out = L.out;
     p.partials = L.partials;
     p.M = M;
+    p.w_rows_b = L.w_batched ? N : 0;
     p.N = N;
     p.K = K;
     p.groups = K / L.group_size;
@@ -1201,7 +1207,8 @@ cudaError_t launch_qmm_tc(const QmmTcLaunch& L, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[which] |= 1ull << dev;
     }
-    dim3 grid((unsigned)L.plan.pieces(), 1u, (unsigned)mchunks);
+    if (B > 65535) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)L.plan.pieces(), (unsigned)B, (unsigned)mchunks);
     return launch_pdl(kern, grid, dim3(kThreads), smem, stream, wmap, xmap, smap, bmap, p);
 }
 

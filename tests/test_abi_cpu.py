@@ -132,10 +132,17 @@ def test_batched_rejects_bad_arguments_without_launching(lib):
 
 def test_batched_workspace_bytes(lib):
     import torch
-    # gather buffer (rounded up to 256 bytes) + the split-K partials of one batch
-    got = g4.gai4_qmm_t_batched_workspace_bytes(3, 33, 4096, 14336, 4, 64, torch.bfloat16, 0)
-    gather = (3 * 33 * 14336 * 2 + 255) // 256 * 256
-    assert got == gather + g4.gai4_qmm_t_workspace_bytes(33, 4096, 14336, 4, 64, torch.bfloat16, 0)
+    # tensor-core path (one launch over the batches): gather buffer (rounded
+    # up to 256 bytes) + split-K partials [S, batch * M, N] for S in 1..4
+    B, M, N, K = 3, 33, 4096, 14336
+    got = g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, 4, 64, torch.bfloat16, 0)
+    gather = (B * M * K * 2 + 255) // 256 * 256
+    parts = got - gather
+    assert parts == 0 or (parts % (B * M * N * 4) == 0 and 2 <= parts // (B * M * N * 4) <= 4)
+    # a forced split: exactly S slots
+    assert g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, 4, 64, torch.bfloat16, 2) == gather + 2 * B * M * N * 4
+    # CUDA-core path (f32): gather + one call's workspace (none)
+    assert g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, 4, 64, torch.float32, 0) == (B * M * K * 4 + 255) // 256 * 256
     assert g4.gai4_qmm_t_batched_workspace_bytes(0, 33, 4096, 14336, 4, 64, torch.bfloat16, 0) == 0
 
 

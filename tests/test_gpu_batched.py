@@ -66,19 +66,21 @@ def test_batched_matches_oracle(dtype, bits, gs, B, M, N, K, stacked, row_pad, b
         assert_within(got[bb], ref, absdot, dtype, f"batch {bb} of {dtype} b{bits} gs{gs} B{B} M{M} N{N} K{K}")
 
 
-def test_batched_equals_single_calls():
-    """Each batch of a batched call equals gai4_qmm_t on that batch's
-    contiguous activations, bit for bit (same plan, same kernels)."""
+@pytest.mark.parametrize("split", [1, 2])
+def test_batched_equals_single_calls(split):
+    """With the same split, each batch of a batched call (one tensor-core
+    launch over all batches) equals gai4_qmm_t on that batch's contiguous
+    activations, bit for bit."""
     dtype, bits, gs, B, M, N, K = "bf16", 4, 64, 3, 24, 512, 2048
     packed, s, b = _weights(B, N, K, bits, gs, dtype, seed=77)
     xs, x = _strided_x(B, M, K, dtype, 78, 40, 2, 5)
     w_dev, s_dev, b_dev = to_dev(np.stack(packed)), to_dev(np.stack(s), dtype), to_dev(np.stack(b), dtype)
-    ws = torch.empty(g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, bits, gs, TORCH_DTYPE[dtype]) // 4 + 64,
-                     dtype=torch.float32, device="cuda")
-    out = g4.gai4_qmm_t_batched(w_dev, s_dev, b_dev, x, bits=bits, group_size=gs, workspace=ws)
+    ws = torch.empty(g4.gai4_qmm_t_batched_workspace_bytes(B, M, N, K, bits, gs, TORCH_DTYPE[dtype], split) // 4
+                     + 64, dtype=torch.float32, device="cuda")
+    out = g4.gai4_qmm_t_batched(w_dev, s_dev, b_dev, x, bits=bits, group_size=gs, split_k=split, workspace=ws)
     for bb in range(B):
-        single_ws = torch.empty(g4.gai4_qmm_t_workspace_bytes(M, N, K, bits, gs, TORCH_DTYPE[dtype], 0) // 4 + 64,
-                                dtype=torch.float32, device="cuda")
+        single_ws = torch.empty(g4.gai4_qmm_t_workspace_bytes(M, N, K, bits, gs, TORCH_DTYPE[dtype], split) // 4
+                                + 64, dtype=torch.float32, device="cuda")
         one = g4.gai4_qmm_t(w_dev[bb], s_dev[bb], b_dev[bb], to_dev(xs[bb], dtype), bits=bits, group_size=gs,
-                            workspace=single_ws)
+                            split_k=split, workspace=single_ws)
         assert torch.equal(out[bb], one), bb
