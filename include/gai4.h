@@ -168,14 +168,19 @@ gai4_status gai4_qmm_t_plan(int64_t M, int64_t N, int64_t K, int bits, int group
  *      need only be aligned to its element size.
  *   out [batch, M, N] T, contiguous.
  * When the activations are not contiguous rows on 16-byte boundaries, one
- * copy kernel first gathers them into `workspace` ([batch, M, K] T); every
- * batch then runs as gai4_qmm_t, in stream order, with the rest of the
- * workspace for its split-K partials (split_k as for gai4_qmm_t).
+ * copy kernel first gathers them into `workspace` ([batch, M, K] T). On the
+ * tensor-core path (as gai4_qmm_t would take for one batch), with the
+ * activations then one [batch * M, K] block, one launch covers every batch
+ * (its split-K partials [S, batch * M, N] in the rest of the workspace, S
+ * planned for all batches together; a forced split_k applies to each batch
+ * and gives each batch's gai4_qmm_t result bit for bit). Otherwise every batch
+ * runs as gai4_qmm_t, in stream order, with the rest of the workspace for its
+ * split-K partials (split_k as for gai4_qmm_t).
  * workspace: device, 16-byte aligned, workspace_bytes >=
  * gai4_qmm_t_batched_workspace_bytes(...) (NULL allowed when that is 0).
- * Errors: as gai4_qmm_t for each batch's arguments (the first failing batch
- * stops the call); GAI4_ERR_INVALID_ARG for batch < 1 or bad strides;
- * GAI4_ERR_WORKSPACE when a gather is needed and the workspace is too small.
+ * Errors: as gai4_qmm_t for the batch's arguments (on the per-batch route the
+ * first failing batch stops the call); GAI4_ERR_INVALID_ARG for batch < 1 or
+ * bad strides; GAI4_ERR_WORKSPACE when the workspace is too small.
  */
 gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* scales, const void* biases, int w_batched,
                                const void* x, int64_t x_batch_stride, int64_t x_row_stride, void* out,
@@ -183,7 +188,8 @@ gai4_status gai4_qmm_t_batched(const uint32_t* w_packed, const void* scales, con
                                int64_t K, int split_k, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace gai4_qmm_t_batched may need: the gathered activations (rounded up
- * to 256 bytes) plus gai4_qmm_t_workspace_bytes(M, N, K, ...) for the splits. */
+ * to 256 bytes) plus the split-K partials: S * batch * M * N * 4 bytes on the
+ * tensor-core path, else gai4_qmm_t_workspace_bytes(M, N, K, ...). */
 size_t gai4_qmm_t_batched_workspace_bytes(int64_t batch, int64_t M, int64_t N, int64_t K, int bits,
                                           int group_size, gai4_dtype dtype, int split_k);
 
