@@ -25,15 +25,18 @@
 //  * The activations are staged once per CTA in shared memory in an order in
 //    which the 32 lanes of a warp read consecutive 16-byte pieces, with the
 //    sum of every 32-element run.
-//  * Decoding places a code in the mantissa of a power of two with one shift
-//    and one three-input logic op, and one packed fp32 fma turns that float
-//    into the exact code; another adds q x. Q8_0: byte b of a word becomes
-//    384 + q (exponent of 256, mantissa bits 15..22 = q + 128 = byte ^ 0x80),
-//    then q = f - 384. Q4_K: one shift places the two nibbles of a byte at
-//    mantissa bits 15..18 and 19..22 of 1.0f, giving 1 + q_lo/256 (sub-block
-//    2g) and 1 + q_hi/16 (sub-block 2g + 1), then (q_lo, q_hi) = (256, 16) f
-//    - (256, 16); the pair accumulates against (x_i, x_{i+32}). Every product
-//    q x is exact before it is summed: a block of zero codes adds exactly 0.
+//  * Every product q x is exact before it is summed: a block of zero codes
+//    adds exactly 0. Q8_0: one shift and one three-input logic op place byte
+//    b of a word in the mantissa of 256 as 384 + q (mantissa bits 15..22 =
+//    q + 128 = byte ^ 0x80), one packed fp32 fma gives q = f - 384, another
+//    adds q x. Q4_K: a nibble masked in place in a code word is a binary32
+//    subnormal, q * 2^(its bit position) * 2^-149 (bit 23, the exponent's
+//    lowest, continues the mantissa seamlessly); byte 3 is shifted down
+//    first. The staged activations carry the inverse power of two of their
+//    nibble's position and a per-item power of two that keeps the products
+//    binary32 normals (down to 2^-103 of the item's largest magnitude), so
+//    one packed fma per byte adds (q_lo x_i, q_hi x_{i+32}): 1 shift, 8 ANDs
+//    and 4 packed fmas per 8 codes; the item's sums are scaled back once.
 //  * Per-row results of a set are held in a small shared buffer and combined
 //    over the sets in a fixed order every F row groups (one consumer barrier
 //    per flush, double-buffered): the result does not depend on timing.
@@ -74,15 +77,10 @@ struct BqArgs {
     long long spin_limit;
 };
 
-// (a & b) ^ c and (a & b) | c as one three-input logic instruction each
+// (a & b) ^ c as one three-input logic instruction
 __device__ __forceinline__ uint32_t lop3_andxor(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
@@ -108,6 +106,20 @@ __device__ __forceinline__ float2 codes2(uint32_t f_lo, uint32_t f_hi, uint32_t 
 }
 __device__ __forceinline__ float2 fma2q(float2 q, float b_lo, float b_hi, float2 c) {
     return ffma2(__float_as_uint(q.x), __float_as_uint(q.y), b_lo, b_hi, c);
+}
+
+// Q4_K: one code word (bytes k = 0..3: low nibble = element 4t + k of the
+// low sub-block, high nibble = of the high one) against its staged,
+// position-scaled activations. A code masked in place is a binary32
+// subnormal (exponent field 0, or 1 for the nibble holding bit 23), i.e.
+// exactly q * 2^(bit position) * 2^-149; byte 3 is moved down first. Each
+// packed fma adds (q_lo x'_lo, q_hi x'_hi) with exact products.
+__device__ __forceinline__ float2 q4k_word(uint32_t w, float4 p0, float4 p1, float2 acc) {
+    const uint32_t h3 = w >> 24;
+    acc = ffma2(w & 0xFu, w & 0xF0u, p0.x, p0.y, acc);
+    acc = ffma2(w & 0xF00u, w & 0xF000u, p0.z, p0.w, acc);
+    acc = ffma2(w & 0xF0000u, w & 0xF00000u, p1.x, p1.y, acc);
+    return ffma2(h3 & 0xFu, h3 & 0xF0u, p1.z, p1.w, acc);
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -213,9 +225,31 @@ __device__ void stage_x(const BqArgs& a, uint8_t* smem) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) lo[j] = hi[j] = 0.f;
             }
+            // the item's scale 2^kc: its largest magnitude's exponent field E -> kc = 253 - E
+            uint32_t eb = 0u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)   // pair quad 4 qq + q: elements i0 + 2q, i0 + 2q + 1
-                xs[(ch * 16 + 4 * qq + q) * 32 + ln] = make_float4(lo[2 * q], hi[2 * q], lo[2 * q + 1], hi[2 * q + 1]);
+            for (int j = 0; j < 8; ++j)
+                eb = max(eb, max(__float_as_uint(lo[j]) & 0x7F800000u, __float_as_uint(hi[j]) & 0x7F800000u));
+            eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 1));
+            eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 2));
+            const int E = max((int)(eb >> 23), 1);
+            const int kc = max(253 - E, -2);
+            // element i (byte i % 4 of its code word): low nibble at bit 8 (i % 4)
+            // (bit 0 for byte 3, after the shift by 24), high nibble 4 bits above;
+            // x staged times 2^(kc - that bit), in two exact power-of-two steps
+            auto scaled = [&](float v, int sh) {
+                const int e = kc - sh;
+                const int ea = e / 2, eb2 = e - e / 2;
+                return (v * __uint_as_float((uint32_t)(127 + ea) << 23)) * __uint_as_float((uint32_t)(127 + eb2) << 23);
+            };
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // pair quad 4 qq + q: elements i0 + 2q, i0 + 2q + 1
+                const int k0 = (i0 + 2 * q) & 3, k1 = (i0 + 2 * q + 1) & 3;
+                const int s0 = k0 == 3 ? 0 : 8 * k0, s1 = k1 == 3 ? 0 : 8 * k1;
+                xs[(ch * 16 + 4 * qq + q) * 32 + ln] =
+                    make_float4(scaled(lo[2 * q], s0), scaled(hi[2 * q], s0 + 4), scaled(lo[2 * q + 1], s1),
+                                scaled(hi[2 * q + 1], s1 + 4));
+            }
             float sl = ((lo[0] + lo[1]) + (lo[2] + lo[3])) + ((lo[4] + lo[5]) + (lo[6] + lo[7]));
             float sh = ((hi[0] + hi[1]) + (hi[2] + hi[3])) + ((hi[4] + hi[5]) + (hi[6] + hi[7]));
             sl += __shfl_xor_sync(0xffffffffu, sl, 1);
@@ -225,6 +259,10 @@ __device__ void stage_x(const BqArgs& a, uint8_t* smem) {
             if (qq == 0) {
                 sums[2 * c] = sl;       // sub-block 2g of super-block 8 ch + sb
                 sums[2 * c + 1] = sh;   // sub-block 2g + 1
+                // the item's code sums come out times 2^(kc - 149): back by 2^p, p = 149 - kc
+                const int pp = 149 - kc;
+                sums[2 * a.chunks * 32 + 2 * c] = __uint_as_float((uint32_t)(127 + pp / 2) << 23);
+                sums[2 * a.chunks * 32 + 2 * c + 1] = __uint_as_float((uint32_t)(127 + pp - pp / 2) << 23);
             }
         }
     }
@@ -319,7 +357,6 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
     const uint32_t ring = smem_u32(smem);
     // loop-invariant logic-op operands, held in registers
     const uint32_t c_mask = pin_reg(FMT == BQ_Q8_0 ? 0x007F8000u : 0x00078000u);
-    const uint32_t c_mask2 = pin_reg(0x00780000u);
     const uint32_t c_const = pin_reg(FMT == BQ_Q8_0 ? 0x43C00000u : 0x3F800000u);
     // code recovery q = m f + c: Q8_0 (1, 1) f + (-384, -384); Q4_K (256, 16) f + (-256, -16)
     const uint32_t r_m_lo = pin_reg(FMT == BQ_Q8_0 ? 0x3F800000u : 0x43800000u);
@@ -402,26 +439,17 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                         for (int t = 0; t < 4; ++t) {
                             const float4 p0 = lds128f(xp + (uint32_t)(8 * h + 2 * t) * 32u * 16u);
                             const float4 p1 = lds128f(xp + (uint32_t)(8 * h + 2 * t + 1) * 32u * 16u);
-                            const uint32_t w = wv[t];
-                            const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
-                            acc = fma2q(codes2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const),
-                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                        p0.x, p0.y, acc);
-                            acc = fma2q(codes2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const),
-                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                        p0.z, p0.w, acc);
-                            acc = fma2q(codes2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const),
-                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                        p1.x, p1.y, acc);
-                            acc = fma2q(codes2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const),
-                                               r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                        p1.z, p1.w, acc);
+                            acc = q4k_word(wv[t], p0, p1, acc);
                         }
                     }
                     const uint4 hdr = lds128(rowa + 144u * (uint32_t)sb);
                     const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
                     float sc_lo, m_lo, sc_hi, m_hi;
                     scale_min_pair(hdr.y, hdr.z, hdr.w, g, sc_lo, m_lo, sc_hi, m_hi);
+                    const float* scl = sums + 2 * a.chunks * 32;   // the item's scale-back factors
+                    const int itm = ch * 32 + 4 * sb + g;
+                    acc.x = (acc.x * scl[2 * itm]) * scl[2 * itm + 1];
+                    acc.y = (acc.y * scl[2 * itm]) * scl[2 * itm + 1];
                     float v = 0.f;
                     v = fmaf(d * sc_lo, acc.x, v);
                     v = fmaf(-(dmin * m_lo), sx_lo, v);
@@ -453,26 +481,16 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
                             const uint32_t wv[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
-                                const uint32_t w = wv[t];
-                                const float4 p0 = xv[2 * t], p1 = xv[2 * t + 1];
-                                const uint32_t u0 = w << 15, u1 = w << 7, u2 = w >> 1, u3 = w >> 9;
-                                acc[r] = fma2q(codes2(lop3_andor(u0, c_mask, c_const), lop3_andor(u0, c_mask2, c_const),
-                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                               p0.x, p0.y, acc[r]);
-                                acc[r] = fma2q(codes2(lop3_andor(u1, c_mask, c_const), lop3_andor(u1, c_mask2, c_const),
-                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                               p0.z, p0.w, acc[r]);
-                                acc[r] = fma2q(codes2(lop3_andor(u2, c_mask, c_const), lop3_andor(u2, c_mask2, c_const),
-                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                               p1.x, p1.y, acc[r]);
-                                acc[r] = fma2q(codes2(lop3_andor(u3, c_mask, c_const), lop3_andor(u3, c_mask2, c_const),
-                                                      r_m_lo, r_m_hi, r_c_lo, r_c_hi),
-                                               p1.z, p1.w, acc[r]);
+                                acc[r] = q4k_word(wv[t], xv[2 * t], xv[2 * t + 1], acc[r]);
                             }
                         }
                     }
+                    const float* scl = sums + 2 * a.chunks * 32;   // this item's scale-back factors
+                    const float sk1 = scl[2 * (ch * 32 + lane)], sk2 = scl[2 * (ch * 32 + lane) + 1];
 #pragma unroll
                     for (int r = 0; r < kR; ++r) {
+                        acc[r].x = (acc[r].x * sk1) * sk2;
+                        acc[r].y = (acc[r].y * sk1) * sk2;
                         const uint4 hdr = lds128(rows + (uint32_t)r * kChunkBytes + 144u * (uint32_t)sb);
                         const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
                         float sc_lo, m_lo, sc_hi, m_hi;
@@ -564,7 +582,7 @@ bool plan_bq(int64_t N, int chunks, int K, int fmt, BqArgs& a, size_t& smem) {
     a.n_groups = (int)((N + kR * a.G - 1) / (kR * a.G));
     a.stage_bytes = (uint32_t)a.C * (uint32_t)(kR * a.G) * kChunkBytes;
     const size_t x_bytes = (size_t)chunks * (fmt == BQ_Q4_K ? 2048 * 4 : (fmt == BQ_Q8_0 ? 1024 * 4 : 1024));
-    const size_t sum_bytes = (size_t)chunks * 32 * (fmt == BQ_Q4_K ? 2 : 1) * 4;
+    const size_t sum_bytes = (size_t)chunks * 32 * (fmt == BQ_Q4_K ? 4 : 1) * 4;   // Q4_K: two sums, two scale factors
     const size_t pend_bytes = (size_t)2 * kFlush * kCW * kR * 4;
     const size_t bar_bytes = 2 * kMaxDepth * 8 + 16;
     const size_t fixed = 128 + x_bytes + sum_bytes + pend_bytes + bar_bytes;

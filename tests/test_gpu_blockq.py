@@ -163,3 +163,32 @@ def test_q4_k_scale_min_decode_bit_exact(decoder):
     for j in range(8):
         pairs = {oracle.q4_k_scale_min(enum[b, 4:16], j) for b in range(j * 4096, (j + 1) * 4096)}
         assert len(pairs) == 4096, j
+
+
+@pytest.mark.parametrize("K", [4096, 5120])   # whole chunks; a last half chunk (lanes take the second row)
+def test_q4_k_x_extreme_ranges(K):
+    """The Q4_K TMA kernel scales each 64-element item of x by a power of two:
+    items of zeros, tiny, huge and very wide-ranged values, and binary32
+    subnormals, against the oracle."""
+    N = 70
+    blocks = synth.q4_k_blocks(N, K, 41)
+    r = np.random.default_rng(42)
+    x = r.standard_normal(K).astype(np.float64)
+    for c in range(K // 64):
+        sl = slice(64 * c, 64 * c + 64)
+        kind = c % 6
+        if kind == 0:
+            x[sl] = 0.0
+        elif kind == 1:
+            x[sl] *= 1e-30
+        elif kind == 2:
+            x[sl] *= 1e30
+        elif kind == 3:
+            x[sl] *= np.where(r.random(64) < 0.5, 1e30, 1e-30)
+        elif kind == 4:
+            x[sl] = r.choice([-1.0, 1.0], 64) * 1e-40 * r.integers(1, 8, 64)
+    x = x.astype(np.float32)
+    ref, absdot = oracle.q4_k_gemv(blocks, x)
+    got = g4.gai4_q4_k_gemv(to_dev(blocks), to_dev(x)).cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert_within(got, ref, absdot, "f32", f"q4_k x extremes K={K}")
