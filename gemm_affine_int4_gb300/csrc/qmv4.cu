@@ -21,7 +21,8 @@
 //    global loads in the loop.
 //  * x is staged once per CTA, permuted so that a warp's 16-byte reads are
 //    contiguous, with per-chunk sums for the bias term: 16-bit activations
-//    as pairs (x_j, x_{j+4}) of the same type, binary32 ones as they are.
+//    as pairs (x_j, x_{j+4}) of the same type, binary32 ones scaled per
+//    element (below).
 //  * Every product q x is exact before it is summed, so a chunk whose codes
 //    are all zero adds exactly zero (no offset is ever subtracted).
 //    16-bit activations: a 16-bit value whose exponent field is 0 or 1 is
@@ -38,12 +39,14 @@
 //    power of two 2^k that puts its largest magnitude in [2^127, 2^128), so
 //    the products are binary32 normals down to 2^-120 of that magnitude, and
 //    the chunk's code sum is scaled back by 2^(133-k).
-//    binary32 activations: code j of a word sits at bits 4j..4j+3 (j < 5)
-//    or, after one 12-bit shift, at bits 8.., 12.., 16..; one logic op ORs it
-//    into a float of exponent 23 - (its bit position), i.e. 2^e + q exactly;
-//    a packed add of (-2^e0, -2^e1) gives the exact pair and a packed fma
-//    adds q * x. Per word: 1 shift, 8 logic ops, 4 packed adds, 4 packed
-//    fmas (fma.rn.f32x2).
+//    binary32 activations: a binary32 whose bits above bit 23 are clear is
+//    those bits times 2^-149 (bit 23 joins the exponent seamlessly), so code
+//    j of a word, masked in place at bits 4j.. (j < 6) or at bits 4 (j - 6)..
+//    of the word shifted by 24, is exactly q_j * 2^(bit - 149). x_j is staged
+//    times 2^(kc - bit), kc chosen per 32-element chunk so that its largest
+//    magnitude lands just below 2^127; a packed fma (fma.rn.f32x2) adds the
+//    exact product q_j x_j 2^(kc - 149), and the chunk's code sum is scaled
+//    back by 2^(149 - kc). Per word: 1 shift, 8 ANDs, 4 packed fmas.
 #include <algorithm>
 #include <initializer_list>
 
@@ -87,13 +90,6 @@ struct Qmv4Args {
     long long spin_limit;
 };
 
-// (a & b) | c as one three-input logic instruction
-__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // (acc.x + a_lo * b_lo, acc.y + a_hi * b_hi): two binary32 fmas in one instruction
 __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo, float b_hi, float2 c) {
     float2 d;
@@ -101,15 +97,6 @@ __device__ __forceinline__ float2 ffma2(uint32_t a_lo, uint32_t a_hi, float b_lo
         " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
         : "=f"(d.x), "=f"(d.y)
         : "r"(a_lo), "r"(a_hi), "f"(b_lo), "f"(b_hi), "f"(c.x), "f"(c.y));
-    return d;
-}
-// (a_lo + b_lo, a_hi + b_hi): exact codes from the floats 2^e + q (every operand a register)
-__device__ __forceinline__ float2 fadd2(uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi) {
-    float2 d;
-    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n add.rn.f32x2 d, a, b;\n"
-        " mov.b64 {%0, %1}, d;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi));
     return d;
 }
 
@@ -254,10 +241,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
             v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
-            xs[((c >> 5) * 8 + 2 * qq) * 32 + (c & 31)] = make_uint4(__float_as_uint(f0.x), __float_as_uint(f0.y),
-                                                                     __float_as_uint(f0.z), __float_as_uint(f0.w));
-            xs[((c >> 5) * 8 + 2 * qq + 1) * 32 + (c & 31)] = make_uint4(
-                __float_as_uint(f1.x), __float_as_uint(f1.y), __float_as_uint(f1.z), __float_as_uint(f1.w));
+            // chunk scale 2^kc: the largest magnitude's exponent field E -> kc = 253 - E
+            uint32_t eb = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) eb = max(eb, __float_as_uint(v[j]) & 0x7F800000u);
+            eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 1));
+            eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 2));
+            const int E = max((int)(eb >> 23), 1);   // subnormal or zero chunk: as E = 1
+            const int kc = max(253 - E, -2);          // Inf / NaN: kept as they are
+            // code j of a word is read in place at bit 4j (j < 6) or, after a shift
+            // by 24, at bit 4 (j - 6): x_j is staged times 2^(kc - that bit), in two
+            // exact power-of-two steps
+            uint32_t xb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = kc - (j < 6 ? 4 * j : 4 * (j - 6));
+                const int ea = e / 2, eb2 = e - e / 2;
+                xb[j] = __float_as_uint((v[j] * __uint_as_float((uint32_t)(127 + ea) << 23)) *
+                                        __uint_as_float((uint32_t)(127 + eb2) << 23));
+            }
+            xs[((c >> 5) * 8 + 2 * qq) * 32 + (c & 31)] = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+            xs[((c >> 5) * 8 + 2 * qq + 1) * 32 + (c & 31)] = make_uint4(xb[4], xb[5], xb[6], xb[7]);
+            if (qq == 0) {
+                // code sums come out times 2^(kc - 149): back by 2^p, p = 149 - kc
+                const int p = 149 - kc;
+                cs[c].y = __uint_as_float((uint32_t)(127 + p / 2) << 23);
+                cs[c].z = __uint_as_float((uint32_t)(127 + p - p / 2) << 23);
+            }
         } else {
             uint4 q = make_uint4(0u, 0u, 0u, 0u);
             if (k0 < K) q = *reinterpret_cast<const uint4*>(xg + k0);
@@ -305,10 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qq == 0) {
             cs[c].x = xsum;
             cs[c].w = 0.f;
-            if constexpr (T::kBytes == 4) {
-                cs[c].y = 1.f;
-                cs[c].z = 1.f;
-            }
         }
     }
     consumer_bar();
@@ -318,13 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // operands of the logic ops and exact subtractions, kept in registers
     constexpr bool kBF = T::kBytes == 2 && T::kIsBF16;
     const uint32_t m2 = pin_reg(0x000F000Fu), mh2 = pin_reg(0x00F000F0u);
-    // binary32: masks of code bits 0.., 4.., 8.., 12.., 16.. and the floats 2^23, 2^19, 2^15, 2^11, 2^7
+    // binary32: masks of code bits 0.., 4.., .., 20..; a masked code is an exact
+    // subnormal, code * 2^(bit - 149)
     const uint32_t f0 = pin_reg(0xFu), f1 = pin_reg(0xF0u), f2 = pin_reg(0xF00u), f3 = pin_reg(0xF000u),
-                   f4 = pin_reg(0xF0000u);
-    const uint32_t e23 = pin_reg(0x4B000000u), e19 = pin_reg(0x49000000u), e15 = pin_reg(0x47000000u),
-                   e11 = pin_reg(0x45000000u), e7 = pin_reg(0x43000000u);
-    const uint32_t n23 = pin_reg(0xCB000000u), n19 = pin_reg(0xC9000000u), n15 = pin_reg(0xC7000000u),
-                   n11 = pin_reg(0xC5000000u), n7 = pin_reg(0xC3000000u);
+                   f4 = pin_reg(0xF0000u), f5 = pin_reg(0xF00000u);
     const int grp_off = (lane * 32) >> a.gs_log2;   // this lane's group within an iteration
     St* out = static_cast<St*>(a.out);
     int slot = 0, ph = 0;
@@ -377,21 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t w = tw == 0 ? wv[r].x : (tw == 1 ? wv[r].y : (tw == 2 ? wv[r].z : wv[r].w));
-                            const uint32_t h = w >> 12;   // codes 5, 6, 7 at bits 8.., 12.., 16..
-                            float2 q;
-                            q = fadd2(lop3_andor(w, f0, e23), lop3_andor(w, f1, e19), n23, n19);
+                            const uint32_t h = w >> 24;   // codes 6, 7 at bits 0.., 4..
                             float2 a2 = acc[r];
-                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p0.x),
-                                       __uint_as_float(p0.y), a2);
-                            q = fadd2(lop3_andor(w, f2, e15), lop3_andor(w, f3, e11), n15, n11);
-                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p0.z),
-                                       __uint_as_float(p0.w), a2);
-                            q = fadd2(lop3_andor(w, f4, e7), lop3_andor(h, f2, e15), n7, n15);
-                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p1.x),
-                                       __uint_as_float(p1.y), a2);
-                            q = fadd2(lop3_andor(h, f3, e11), lop3_andor(h, f4, e7), n11, n7);
-                            a2 = ffma2(__float_as_uint(q.x), __float_as_uint(q.y), __uint_as_float(p1.z),
-                                       __uint_as_float(p1.w), a2);
+                            a2 = ffma2(w & f0, w & f1, __uint_as_float(p0.x), __uint_as_float(p0.y), a2);
+                            a2 = ffma2(w & f2, w & f3, __uint_as_float(p0.z), __uint_as_float(p0.w), a2);
+                            a2 = ffma2(w & f4, w & f5, __uint_as_float(p1.x), __uint_as_float(p1.y), a2);
+                            a2 = ffma2(h & f0, h & f1, __uint_as_float(p1.z), __uint_as_float(p1.w), a2);
                             acc[r] = a2;
                         }
                     }
@@ -402,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (T::kBytes == 2)
                         qx = (fmaf(0.0625f, acc[r].y, acc[r].x) * cst.y) * cst.z;
                     else
-                        qx = acc[r].x + acc[r].y;
+                        qx = ((acc[r].x + acc[r].y) * cst.y) * cst.z;
                     part[r] = fmaf(sc[r], qx, fmaf(bc[r], cst.x, part[r]));
                 }
             } else {

@@ -188,7 +188,7 @@ def _x_extremes(K, dtype, seed):
     """x whose 32-element chunks are: all zero, tiny, huge, spanning many
     binades, subnormal in the type, and ordinary N(0, 1)."""
     r = np.random.default_rng(seed)
-    big, small, sub = (1e30, 1e-30, 1e-39) if dtype == "bf16" else (2e4, 1e-4, 3e-7)
+    big, small, sub = (2e4, 1e-4, 3e-7) if dtype == "f16" else (1e30, 1e-30, 1e-39)
     x = r.standard_normal(K).astype(np.float64)
     for c in range(K // 32):
         sl = slice(32 * c, 32 * c + 32)
@@ -207,15 +207,18 @@ def _x_extremes(K, dtype, seed):
 
 
 def _bits_of(x32, dtype):
+    if dtype == "f32":
+        return x32
     t = torch.from_numpy(x32).to(TORCH_DTYPE[dtype])
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("gs", [32, 64, 128])
 def test_qmv_4bit_x_extreme_ranges(dtype, gs):
     """The 4-bit qmv kernel on x with zero, tiny, huge, wide-range and
-    subnormal chunks (the bf16 path scales each chunk by a power of two)."""
+    subnormal chunks (the bf16 and binary32 paths scale each chunk by a
+    power of two)."""
     N, K = 96, 4096
     _, packed, s, b, _ = affine_problem(N, K, 1, 4, gs, dtype, seed=gs + 5)
     x = _x_extremes(K, dtype, gs)
