@@ -293,26 +293,26 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
         const int lim = min((s + 1) * a.cps, a.chunks);
         return max(0, min(C, lim - c0));
     };
-    // Warm L2 with the first ring-full of stages while the barriers are set up
-    // and the kernels before this one finish; the copies start after that wait.
+    // Warm L2 with x first (at the head of the DRAM queue) and fetch the
+    // tensor map while the barriers are set up
     if (warp == kCW && lane == 0) {
+        // K % 32 == 0: whole 16-byte units (int8 codes or binary32 x)
+        if constexpr (FMT == BQ_Q8_0_I8)
+            bulk_prefetch_l2(a.xq, (uint32_t)a.K);
+        else
+            bulk_prefetch_l2(a.x, (uint32_t)a.K * 4u);
         asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
-        int cnt = 0;
-        for (int rg = blockIdx.x; rg < a.n_groups && cnt < D; rg += gridDim.x)
-            for (int ks = 0; ks < a.kss && cnt < D; ++ks)
-                for (int s = 0; s < S && cnt < D; ++s, ++cnt) {
-                    int c0;
-                    const int n = stage_chunks(s, ks, c0);
-                    for (int c = 0; c < n; ++c) tma_prefetch_2d(&wmap, (c0 + c) * kChunkU64, rg * (kR * G));
-                }
     }
     __syncthreads();   // barriers initialised: the producer starts while the consumers stage x
-    pdl_wait();        // the kernels before this one are complete: global memory may be read
     Ctl ctl{a.status, a.spin_limit, abort_flag};
 
     if (warp == kCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
+            // The blocks are not written by the kernels this one may overlap
+            // (programmatic launch): the first ring-full of stages is
+            // requested at once, before those kernels complete. Only the
+            // activations wait for them.
             int slot = 0, ph = 0, issued = 0;
             bool ok = true;
             for (int rg = blockIdx.x; rg < a.n_groups && ok; rg += gridDim.x) {
@@ -345,6 +345,7 @@ __device__ __forceinline__ void bq_tma_body(const CUtensorMap& wmap, const BqArg
     }
 
     // ---------------- consumers ----------------
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
     stage_x<FMT>(a, smem);
     consumer_bar();
     // warp wg of set s: rows kR * wg .. kR * wg + kR - 1 of every stage of the

@@ -17,8 +17,11 @@ namespace gai4 {
 // the next kernel in the stream may start (its launch and set-up: barriers,
 // tensor-memory allocation) while this one finishes: every kernel lets its
 // dependents be scheduled at entry, and waits for the kernels before it to
-// complete -- with their memory visible -- before its first global-memory
-// access. A kernel that reads another call's output is therefore ordered
+// complete -- with their memory visible -- before it reads activations or
+// writes any output or workspace. The streaming GEMV / GEMM kernels read the
+// packed weights (which no kernel of the library writes, and no kernel that
+// does not signal programmatic launch can still be writing) before that
+// wait. A kernel that reads another call's output is therefore ordered
 // exactly as with plain stream order.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -118,17 +118,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// L2 prefetch of a tensor box (no shared-memory write, no barrier). It only
-// warms the coherent L2, so it may be issued before the kernels this one
-// depends on have completed.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
-                 "r"(z)
-                 : "memory");
+// L2 prefetch of a contiguous byte range (16-byte aligned start, a multiple of
+// 16 bytes), in pieces of at most 32 KB. It only warms the coherent L2, so it
+// may be issued before the kernels this one depends on have completed; issued
+// before the weight copies, it puts the activations at the head of the DRAM
+// queue.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    const char* c = static_cast<const char*>(p);
+    for (uint32_t o = 0; o < bytes; o += 32768u) {
+        const uint32_t n = bytes - o < 32768u ? bytes - o : 32768u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"(n) : "memory");
+    }
 }
 
 }  // namespace pipe

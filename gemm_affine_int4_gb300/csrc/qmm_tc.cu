@@ -577,26 +577,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nxs = (nk64 + 1) / 2;                            // 128-column activation stages
     const int nas = nxs;                                       // = A stages
 
-    // Warm L2 with the first ring-full of weight stages (and their scales /
-    // biases) while the barriers and tensor memory are set up and the kernels
-    // before this one finish; the copies themselves start after that wait.
-    if (warp == 1 && lane == 0) {
-        for (int i = 0; i < nst && i < WS; ++i) {
-            const int64_t kst = k_begin + (int64_t)kBK * i;
-            tma_prefetch_2d(&wmap, (int)(kst * BITS / 32), (int)nw0);
-            if constexpr (BITS == 6 || BITS == 8) tma_prefetch_2d(&wmap, (int)(kst * BITS / 32) + 4 * BITS, (int)nw0);
-            if constexpr (SBT) {
-                int x0 = 0, nbox = 0;
-                stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
-                for (int bx = 0; bx < nbox; ++bx) {
-                    tma_prefetch_2d(&smap, x0 + 8 * bx, (int)nw0);
-                    tma_prefetch_2d(&bmap, x0 + 8 * bx, (int)nw0);
-                }
+    // the copy of weight stage i (and its scales / biases) into ring slot i % WS
+    auto issue_w = [&](int i) {
+        const int s = i % WS;
+        const int64_t kst = k_begin + (int64_t)kBK * i;
+        int x0 = 0, nbox = 0;
+        if constexpr (SBT) stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
+        mbar_arrive_expect_tx(&w_full[s], w_stage_bytes + 2u * kSbBox * (uint32_t)nbox);
+        // x coordinate in 32-bit words: (k_begin + 256 i) * BITS / 32; 6- and
+        // 8-bit stages come as two 128-column boxes
+        tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst * BITS / 32), (int)nw0);
+        if constexpr (BITS == 6 || BITS == 8)
+            tma_load_2d(wbuf + (size_t)s * w_stage_bytes + w_stage_bytes / 2, &wmap, &w_full[s],
+                        (int)(kst * BITS / 32) + 4 * BITS, (int)nw0);
+        if constexpr (SBT) {
+            uint8_t* sb = sbbuf + (size_t)s * sb_stage_bytes;
+            for (int bx = 0; bx < nbox; ++bx) {
+                tma_load_2d(sb + bx * kSbBox, &smap, &w_full[s], x0 + 8 * bx, (int)nw0);
+                tma_load_2d(sb + (uint32_t)p.sb_boxes * kSbBox + bx * kSbBox, &bmap, &w_full[s], x0 + 8 * bx,
+                            (int)nw0);
             }
         }
-    }
+    };
 
-    if (threadIdx.x == 0) {
+    if (warp == 1 && lane == 0) {   // (warp 0 allocates tensor memory meanwhile)
         for (int i = 0; i < WS; ++i) {
             mbar_init(&w_full[i], 1);
             mbar_init(&w_empty[i], 8);   // both halves: one arrive per warp of two groups
@@ -612,6 +616,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, p.n_issuers);         // one commit per issuer
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the barriers, as the copies see them
+        // Programmatic launch: this kernel may start while the kernels before
+        // it finish. The packed weights, scales and biases are not written by
+        // them, so the first ring-full of weight stages is requested now,
+        // before the tensor-memory set-up; the activation copies and every
+        // global store wait for those kernels to complete.
+        for (int i = 0; i < nst && i < WS; ++i) issue_w(i);
     }
     if (warp == 0) {   // tensor-memory allocation (whole warp)
         __syncwarp();
@@ -624,7 +635,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();   // the kernels before this one are complete: global memory may be read
     const uint32_t acc_col = 0;   // accumulator of issuer j: columns [j * mt, (j + 1) * mt)
     const int NI = p.n_issuers;
     const uint32_t a_col0 = (uint32_t)kTmemCols - kAStageCols * (uint32_t)AS;   // A ring at the top
@@ -633,28 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- packed-weight producer ----------------
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % WS;
-                if (!mbar_wait(&w_empty[s], ((i / WS) & 1) ^ 1, ctl)) break;
-                const int64_t kst = k_begin + (int64_t)kBK * i;
-                int x0 = 0, nbox = 0;
-                if constexpr (SBT) stage_groups(kst, (int)min((int64_t)kBK, k_end - kst), p.gs_log2, x0, nbox);
-                mbar_arrive_expect_tx(&w_full[s], w_stage_bytes + 2u * kSbBox * (uint32_t)nbox);
-                // x coordinate in 32-bit words: (k_begin + 256 i) * BITS / 32; 6- and
-                // 8-bit stages come as two 128-column boxes
-                tma_load_2d(wbuf + (size_t)s * w_stage_bytes, &wmap, &w_full[s], (int)(kst * BITS / 32), (int)nw0);
-                if constexpr (BITS == 6 || BITS == 8)
-                    tma_load_2d(wbuf + (size_t)s * w_stage_bytes + w_stage_bytes / 2, &wmap, &w_full[s],
-                                (int)(kst * BITS / 32) + 4 * BITS, (int)nw0);
-                if constexpr (SBT) {
-                    uint8_t* sb = sbbuf + (size_t)s * sb_stage_bytes;
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        tma_load_2d(sb + bx * kSbBox, &smap, &w_full[s], x0 + 8 * bx, (int)nw0);
-                        tma_load_2d(sb + (uint32_t)p.sb_boxes * kSbBox + bx * kSbBox, &bmap, &w_full[s], x0 + 8 * bx,
-                                    (int)nw0);
-                    }
-                }
+            int issued = min(nst, WS);   // the first ring-full went out before the set-up
+            for (int i = issued; i < nst; ++i) {
+                if (!mbar_wait(&w_empty[i % WS], ((i / WS) & 1) ^ 1, ctl)) break;
+                issue_w(i);
                 ++issued;
             }
             // drain: every issued copy has landed before the CTA may exit
@@ -664,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- activation producer ----------------
         if (lane == 0) {
+            pdl_wait();   // the kernels before this one are complete: x may be read
             int issued = 0;
             for (int j = 0; j < nxs; ++j) {
                 const int s = j % XS;
@@ -940,6 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // epilogue: accumulator rows -> fp32 partials or T output; the 4 warps
         // of a quadrant take 8-column chunks in turn
+        pdl_wait();   // the kernels before this one are complete: the output and partials may be written
         const bool ok = warp_wait(acc_full, 0, ctl);
         fence_after();
         if (ok) {

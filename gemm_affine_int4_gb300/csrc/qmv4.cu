@@ -143,85 +143,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t my_blocks =
         a.n_blocks > (int64_t)blockIdx.x ? (a.n_blocks - 1 - (int64_t)blockIdx.x) / gridDim.x + 1 : 0;
 
-    // Warm L2 with the first ring-full of stages while the barriers are set up
-    // and the kernels before this one finish; the copies start after that wait.
-    if (warp == kCWarps && lane == 0) {
-        int cnt = 0;
-        for (int64_t b = 0; b < my_blocks && cnt < D; ++b) {
-            const int row0 = (int)(((int64_t)blockIdx.x + b * gridDim.x) * BR);
-            for (int j = 0; j < n_st && cnt < D; ++j, ++cnt) {
-                const int it0 = j * S;
-                const int nsl = min(S, n_it - it0);
-                if (a.box3) {
-                    tma_prefetch_3d(&wmap, 0, it0, row0);
-                    tma_prefetch_3d(&smap, 0, it0, row0);
-                    tma_prefetch_3d(&bmap, 0, it0, row0);
-                } else {
-                    for (int ss = 0; ss < nsl; ++ss) {
-                        const int it = it0 + ss;
-                        tma_prefetch_2d(&wmap, it * (kItCols / 8), row0);
-                        tma_prefetch_2d(&smap, it * a.sbg, row0);
-                        tma_prefetch_2d(&bmap, it * a.sbg, row0);
-                    }
-                }
-            }
-        }
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < D; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kCWarps);   // one arrive per consumer warp
-        }
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    pdl_wait();   // the kernels before this one are complete: global memory may be read
     Ctl ctl{a.status, a.spin_limit, abort_flag};
 
     if (warp == kCWarps) {
         // ---------------- producer ----------------
-        if (lane == 0) {
-            int slot = 0, ph = 0;
-            int64_t issued = 0;
-            for (int64_t b = 0; b < my_blocks; ++b) {
-                const int row0 = (int)(((int64_t)blockIdx.x + b * gridDim.x) * BR);
-                for (int j = 0; j < n_st; ++j) {
-                    if (!mbar_wait(&empty[slot], (uint32_t)(ph ^ 1), ctl)) goto drain;
-                    const int it0 = j * S;
-                    const int nsl = min(S, n_it - it0);   // iterations present in this stage
-                    // a 3-D box always lands whole (iterations past the row are zero-filled)
-                    const uint32_t n_its = a.box3 ? (uint32_t)S : (uint32_t)nsl;
-                    mbar_arrive_expect_tx(&full[slot],
-                                          n_its * (a.w_slice + 2u * (uint32_t)BR * (uint32_t)a.sbg *
-                                                                   (uint32_t)sizeof(St)));
-                    uint8_t* st = ring + (size_t)slot * a.stage_bytes;
-                    if (a.box3) {
-                        tma_load_3d(st, &wmap, &full[slot], 0, it0, row0);
-                        uint8_t* sbs = st + (size_t)S * a.w_slice;
-                        tma_load_3d(sbs, &smap, &full[slot], 0, it0, row0);
-                        tma_load_3d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], 0, it0, row0);
-                    } else for (int ss = 0; ss < nsl; ++ss) {
-                        const int it = it0 + ss;
-                        tma_load_2d(st + ss * a.w_slice, &wmap, &full[slot], it * (kItCols / 8), row0);
-                        uint8_t* sbs = st + (size_t)S * a.w_slice + (size_t)ss * a.sb_slice;
-                        tma_load_2d(sbs, &smap, &full[slot], it * a.sbg, row0);
-                        tma_load_2d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], it * a.sbg, row0);
-                    }
-                    ++issued;
-                    if (++slot == D) {
-                        slot = 0;
-                        ph ^= 1;
-                    }
-                }
+        // stage q of this CTA (block q / n_st, iterations S (q % n_st) ..)
+        // into ring slot q % D
+        auto issue = [&](int64_t q) {
+            const int64_t b = q / n_st;
+            const int j = (int)(q - b * n_st), slot = (int)(q % D);
+            const int row0 = (int)(((int64_t)blockIdx.x + b * gridDim.x) * BR);
+            const int it0 = j * S;
+            const int nsl = min(S, n_it - it0);   // iterations present in this stage
+            // a 3-D box always lands whole (iterations past the row are zero-filled)
+            const uint32_t n_its = a.box3 ? (uint32_t)S : (uint32_t)nsl;
+            mbar_arrive_expect_tx(&full[slot],
+                                  n_its * (a.w_slice + 2u * (uint32_t)BR * (uint32_t)a.sbg * (uint32_t)sizeof(St)));
+            uint8_t* st = ring + (size_t)slot * a.stage_bytes;
+            if (a.box3) {
+                tma_load_3d(st, &wmap, &full[slot], 0, it0, row0);
+                uint8_t* sbs = st + (size_t)S * a.w_slice;
+                tma_load_3d(sbs, &smap, &full[slot], 0, it0, row0);
+                tma_load_3d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], 0, it0, row0);
+            } else for (int ss = 0; ss < nsl; ++ss) {
+                const int it = it0 + ss;
+                tma_load_2d(st + ss * a.w_slice, &wmap, &full[slot], it * (kItCols / 8), row0);
+                uint8_t* sbs = st + (size_t)S * a.w_slice + (size_t)ss * a.sb_slice;
+                tma_load_2d(sbs, &smap, &full[slot], it * a.sbg, row0);
+                tma_load_2d(sbs + (size_t)S * a.sb_slice, &bmap, &full[slot], it * a.sbg, row0);
             }
-        drain:
+        };
+        const int64_t total = my_blocks * n_st;
+        int64_t issued = 0;
+        if (lane == 0) {
+            // x first into L2 (at the head of the DRAM queue), then the tensor maps
+            bulk_prefetch_l2(a.x, (uint32_t)(a.K * (int64_t)sizeof(St)));   // K % 32 == 0: whole 16-byte units
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&smap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
+            for (int i = 0; i < D; ++i) {
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], kCWarps);   // one arrive per consumer warp
+            }
+            *abort_flag = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the barriers, as the copies see them
+            // The packed weights, scales and biases are not written by the
+            // kernels this one may overlap (programmatic launch): the first
+            // ring-full of stages is requested at once, before those kernels
+            // complete. Only the activations wait for them.
+            for (; issued < total && issued < D; ++issued) issue(issued);
+        }
+        __syncwarp();
+        __syncthreads();   // the barriers are initialised (and the consumers have staged x)
+        if (lane == 0) {
+            for (; issued < total; ++issued) {
+                if (!mbar_wait(&empty[issued % D], (uint32_t)(((issued / D) & 1) ^ 1), ctl)) break;
+                issue(issued);
+            }
             // every issued copy has landed before the CTA may exit
             for (int64_t q = (issued > D ? issued - D : 0); q < issued; ++q)
                 mbar_wait_drain(&full[q % D], (uint32_t)((q / D) & 1), a.spin_limit, a.status);
         }
         return;
     }
+
+    pdl_wait();   // the kernels before this one are complete: global memory may be read
 
     // ---------------- consumers: stage x once ----------------
     // a thread takes 8 consecutive elements (word qq of a 32-element chunk);
@@ -317,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cs[c].w = 0.f;
         }
     }
-    consumer_bar();
+    __syncthreads();   // x staged; the ring's barriers are initialised
 
     // ---------------- consumers: main loop ----------------
     const int g = warp / S, sl = warp % S;

@@ -11,6 +11,14 @@
  *    device-side state is one status word per device (see
  *    gai4_last_device_status) and the fixed scratch array of
  *    gai4_qmm_t_noalloc, both static __device__ variables.
+ *  - Kernels are launched with programmatic dependent launch: a call may
+ *    start while the kernel before it in the stream finishes, if that kernel
+ *    allows it (this library's kernels do; a kernel that does not signal it
+ *    is waited for in full, as usual). The packed weights, scales, biases and
+ *    quantized blocks may be read from the start of the call; activations are
+ *    read, and outputs and workspaces written, only after the preceding
+ *    kernels have completed. So a kernel that writes weights must not signal
+ *    programmatic launch before those writes are complete.
  *  - Arguments are validated on the host before anything is launched. A call
  *    that returns anything but GAI4_OK has launched nothing and written nothing.
  *  - Outputs are fully overwritten (no accumulate-into mode).
