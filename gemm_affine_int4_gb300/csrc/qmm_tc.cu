@@ -619,10 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the barriers, as the copies see them
         // Programmatic launch: this kernel may start while the kernels before
         // it finish. The packed weights, scales and biases are not written by
-        // them, so the first ring-full of weight stages is requested now,
-        // before the tensor-memory set-up; the activation copies and every
-        // global store wait for those kernels to complete.
-        for (int i = 0; i < nst && i < WS; ++i) issue_w(i);
+        // them, so the first weight stage is requested now, before the
+        // tensor-memory set-up (the rest of the ring follows after it:
+        // requested alone, the first stage lands sooner); the activation
+        // copies and every global store wait for those kernels to complete.
+        if (nst > 0) issue_w(0);
     }
     if (warp == 0) {   // tensor-memory allocation (whole warp)
         __syncwarp();
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- packed-weight producer ----------------
         if (lane == 0) {
-            int issued = min(nst, WS);   // the first ring-full went out before the set-up
+            int issued = min(nst, 1);   // the first stage went out before the set-up
             for (int i = issued; i < nst; ++i) {
                 if (!mbar_wait(&w_empty[i % WS], ((i / WS) & 1) ^ 1, ctl)) break;
                 issue_w(i);

@@ -190,9 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the barriers, as the copies see them
             // The packed weights, scales and biases are not written by the
             // kernels this one may overlap (programmatic launch): the first
-            // ring-full of stages is requested at once, before those kernels
-            // complete. Only the activations wait for them.
-            for (; issued < total && issued < D; ++issued) issue(issued);
+            // stage is requested at once, before those kernels complete (the
+            // rest of the ring follows once the CTA is set up: requested
+            // alone, the first stage lands sooner). Only the activations wait
+            // for those kernels.
+            if (total > 0) issue(issued++);
         }
         __syncwarp();
         __syncthreads();   // the barriers are initialised (and the consumers have staged x)
