@@ -12,6 +12,10 @@
 // Neither block size is a multiple of four bytes, so a block cannot be read in
 // place with aligned word loads. Each warp owns one output row at a time and
 // walks it in slabs of whole blocks (one contiguous run of the row's bytes).
+// x is staged once per CTA in shared memory when it fits (K up to 24576),
+// otherwise read through the read-only cache; the first slabs of the blocks
+// are requested before the kernels this one overlaps complete (they never
+// write blocks), x only after.
 // A slab is copied by 16-byte asynchronous copies (cp.async, L2-only), starting
 // at the 16-byte boundary at or below it, into a warp-private ring of
 // shared-memory stages kStages - 1 slabs ahead of the decode (the copy that
@@ -26,8 +30,11 @@
 // (Q6_K), and a warp-shuffle sum finishes each row.
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace gai4 {
 namespace {
@@ -51,7 +58,17 @@ struct GgufFmt<1> {   // Q6_K, 210-byte super-blocks
 // room for the one-word overread of a re-aligned load past the slab's last byte
 static_assert(32 * 34 + 15 + 4 <= 3 * 32 * 16, "Q8_0 slab");
 static_assert(8 * 210 + 15 + 4 <= 4 * 32 * 16, "Q6_K slab");
-static_assert(kWarps * 4 * 3 * 512 <= 48 * 1024 && kWarps * 3 * 4 * 512 <= 48 * 1024, "static shared memory");
+static_assert(kWarps * 4 * 3 * 512 <= 48 * 1024 && kWarps * 3 * 4 * 512 <= 48 * 1024, "ring of stages");
+constexpr int64_t kMaxSmemX = 24576;   // largest K whose binary32 x is staged in shared memory
+
+// 16 bytes of x: from shared memory (staged) or through the read-only cache
+template <bool XSM>
+__device__ __forceinline__ float4 ld_x4(const float* p) {
+    if constexpr (XSM)
+        return *reinterpret_cast<const float4*>(p);
+    else
+        return __ldg(reinterpret_cast<const float4*>(p));
+}
 
 // the 32-bit word at a 2-byte-aligned shared-memory offset
 __device__ __forceinline__ uint32_t lds_u32_at(const uint8_t* buf, int o) {
@@ -81,10 +98,11 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // sum over slab `slab` of one Q8_0 row: 8 lanes per block (4 codes each), 4
 // blocks per pass
-__device__ __forceinline__ float decode_q8_0_34(const uint8_t* buf, int m, const float* __restrict__ x,
-                                                int64_t slab, int64_t nb, int lane) {
-    const int64_t b0 = slab * GgufFmt<0>::kSB;
-    const int nbs = (int)min((int64_t)GgufFmt<0>::kSB, nb - b0);
+template <bool XSM>
+__device__ __forceinline__ float decode_q8_0_34(const uint8_t* buf, int m, const float* __restrict__ x, int slab,
+                                                int nb, int lane) {
+    const int b0 = slab * GgufFmt<0>::kSB;
+    const int nbs = min(GgufFmt<0>::kSB, nb - b0);
     const int e4 = (lane & 7) * 4;
     const float off = 8388736.0f;   // 2^23 + 128
     float acc = 0.f;
@@ -93,7 +111,7 @@ __device__ __forceinline__ float decode_q8_0_34(const uint8_t* buf, int m, const
         const int o = m + 34 * jb;
         const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(buf + o));
         const uint32_t w = lds_u32_at(buf, o + 2 + e4) ^ 0x80808080u;
-        const float4 xv = __ldg(reinterpret_cast<const float4*>(x + (b0 + jb) * 32 + e4));
+        const float4 xv = ld_x4<XSM>(x + (b0 + jb) * 32 + e4);
         float s = code_f<0>(w, off) * xv.x;
         s = fmaf(code_f<1>(w, off), xv.y, s);
         s = fmaf(code_f<2>(w, off), xv.z, s);
@@ -109,10 +127,11 @@ __device__ __forceinline__ float decode_q8_0_34(const uint8_t* buf, int m, const
 // (k < 4); the high bit pairs of both sit in qh bytes 32h + r % 32 + k, at
 // bits 2c and 2c + 4 (c = r / 32); the scales are sc[8h + r/16] and
 // sc[8h + 4 + r/16].
-__device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const float* __restrict__ x,
-                                             int64_t slab, int64_t nb, int lane) {
-    const int64_t b0 = slab * GgufFmt<1>::kSB;
-    const int nbs = (int)min((int64_t)GgufFmt<1>::kSB, nb - b0);
+template <bool XSM>
+__device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const float* __restrict__ x, int slab,
+                                             int nb, int lane) {
+    const int b0 = slab * GgufFmt<1>::kSB;
+    const int nbs = min(GgufFmt<1>::kSB, nb - b0);
     const int h = lane >> 4, r = (lane & 15) * 4;
     const int csh = (r >> 5) * 2;
     const float off = 8388640.0f;   // 2^23 + 32
@@ -126,8 +145,8 @@ __device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const fl
         const float sh = (float)(int8_t)buf[o + 196 + 8 * h + (r >> 4)];
         const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(buf + o + 208));
         const float* xb = x + (b0 + jb) * 256 + 128 * h + r;
-        const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
-        const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 64));
+        const float4 xl = ld_x4<XSM>(xb);
+        const float4 xh = ld_x4<XSM>(xb + 64);
         const uint32_t lo = (qlw & 0x0F0F0F0Fu) | ((q2 << 4) & 0x30303030u);
         const uint32_t hi = ((qlw >> 4) & 0x0F0F0F0Fu) | (q2 & 0x30303030u);
         float a = code_f<0>(lo, off) * xl.x;
@@ -143,36 +162,36 @@ __device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const fl
     return acc;
 }
 
-template <int FMT>
+template <int FMT, bool XSM>
 __global__ void __launch_bounds__(kWarps * 32) gguf_gemv_kernel(const uint8_t* __restrict__ blocks,
                                                                 const float* __restrict__ x, float* __restrict__ out,
                                                                 int64_t N, int64_t nb, int64_t total) {
     using F = GgufFmt<FMT>;
     constexpr int kStageBytes = F::kCPL * 512;
+    extern __shared__ __align__(16) uint8_t gg_smem[];
     pdl_launch_dependents();
-    pdl_wait();   // the kernels before this one are complete: global memory may be read
-    __shared__ __align__(16) uint8_t sbuf[kWarps][F::kStages][kStageBytes];
+    // [kWarps][kStages][kStageBytes] ring, then (XSM) x [K] binary32
+    uint8_t (*sbuf)[F::kStages][kStageBytes] = reinterpret_cast<uint8_t (*)[F::kStages][kStageBytes]>(gg_smem);
+    float* xs = reinterpret_cast<float*>(gg_smem + (size_t)kWarps * F::kStages * kStageBytes);
+    const int64_t K = nb * F::kBK;
+    if (XSM && threadIdx.x == 0) pipe::bulk_prefetch_l2(x, (uint32_t)(K * 4));   // x to the head of the DRAM queue
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t nslab = (nb + F::kSB - 1) / F::kSB;
+    const int nslab = (int)((nb + F::kSB - 1) / F::kSB);
     const int64_t wstride = (int64_t)gridDim.x * kWarps;
     const int64_t RB = nb * F::kBB;
     const int64_t row0 = (int64_t)blockIdx.x * kWarps + warp;
-    // this warp's items: slab t % nslab of row row0 + (t / nslab) * wstride
-    const int64_t n_items = row0 < N ? ((N - 1 - row0) / wstride + 1) * nslab : 0;
+    // this warp's items: slabs 0 .. nslab - 1 of rows row0, row0 + wstride, ...
+    // walked by two cursors (row, slab): the next item to copy, the next to decode
 
-    // byte offset of item t's first block in the block array
-    auto item_start = [&](int64_t t) {
-        const int64_t r = row0 + (t / nslab) * wstride, s = t % nslab;
-        return r * RB + s * F::kSB * F::kBB;
-    };
-    auto issue = [&](int64_t t) {
-        if (t < n_items) {
-            const int64_t s = t % nslab;
-            const int64_t nbs = min((int64_t)F::kSB, nb - s * F::kSB);
-            const int64_t start = item_start(t);
+    int64_t ir = row0;   // copy cursor
+    int is = 0, islot = 0;
+    auto issue = [&]() {
+        if (ir < N) {
+            const int nbs = (int)min((int64_t)F::kSB, nb - (int64_t)is * F::kSB);
+            const int64_t start = ir * RB + (int64_t)is * (F::kSB * F::kBB);
             const int64_t a0 = start & ~(int64_t)15;
-            const int nch = (int)((start - a0 + nbs * F::kBB + 15) >> 4);
-            uint8_t* st = sbuf[warp][t % F::kStages];
+            const int nch = ((int)(start - a0) + nbs * F::kBB + 15) >> 4;
+            uint8_t* st = sbuf[warp][islot];
 #pragma unroll
             for (int i = 0; i < F::kCPL; ++i) {
                 const int c = i * 32 + lane;
@@ -181,30 +200,46 @@ __global__ void __launch_bounds__(kWarps * 32) gguf_gemv_kernel(const uint8_t* _
                     cp_async16(st + 16 * c, blocks + g, (int)min((int64_t)16, total - g));
                 }
             }
+            if (++is == nslab) {
+                is = 0;
+                ir += wstride;
+            }
         }
         cp_async_commit();   // one group per item (empty past the end) keeps the counting uniform
+        if (++islot == F::kStages) islot = 0;
     };
 
 #pragma unroll
-    for (int t = 0; t < F::kStages - 1; ++t) issue(t);
+    for (int t = 0; t < F::kStages - 1; ++t) issue();   // blocks: before the wait
+    pdl_wait();   // the kernels before this one are complete: x may be read, out written
+    const float* xr = x;
+    if constexpr (XSM) {
+        const float4* xg4 = reinterpret_cast<const float4*>(x);
+        float4* xs4 = reinterpret_cast<float4*>(xs);
+        for (int64_t i = threadIdx.x; i < K / 4; i += kWarps * 32) xs4[i] = __ldg(xg4 + i);
+        __syncthreads();
+        xr = xs;
+    }
     float acc = 0.f;
-    for (int64_t t = 0; t < n_items; ++t) {
-        __syncwarp();                  // every lane is done with the stage item t - 1 used
-        issue(t + F::kStages - 1);     // ... which item t + kStages - 1 now refills
+    int cslot = 0;
+    for (int64_t cr = row0, cs = 0; cr < N;) {   // decode cursor
+        __syncwarp();                  // every lane is done with the stage the previous item used
+        issue();                       // ... which the item kStages - 1 ahead now refills
         cp_async_wait<F::kStages - 1>();
-        __syncwarp();                  // item t's chunks from every lane have landed
-        const uint8_t* buf = sbuf[warp][t % F::kStages];
-        const int64_t start = item_start(t);
-        const int m = (int)(start & 15);
-        const int64_t s = t % nslab;
+        __syncwarp();                  // this item's chunks from every lane have landed
+        const uint8_t* buf = sbuf[warp][cslot];
+        const int m = (int)((cr * RB + cs * (F::kSB * F::kBB)) & 15);
         if constexpr (FMT == 0)
-            acc += decode_q8_0_34(buf, m, x, s, nb, lane);
+            acc += decode_q8_0_34<XSM>(buf, m, xr, (int)cs, (int)nb, lane);
         else
-            acc += decode_q6_k(buf, m, x, s, nb, lane);
-        if (s == nslab - 1) {
+            acc += decode_q6_k<XSM>(buf, m, xr, (int)cs, (int)nb, lane);
+        if (++cslot == F::kStages) cslot = 0;
+        if (++cs == nslab) {
             const float v = warp_sum(acc);
-            if (lane == 0) out[row0 + (t / nslab) * wstride] = v;
+            if (lane == 0) out[cr] = v;
             acc = 0.f;
+            cs = 0;
+            cr += wstride;
         }
     }
     cp_async_wait<0>();   // no copy outlives the warp (the trailing groups are empty)
@@ -217,9 +252,24 @@ cudaError_t launch_gguf_gemv(const uint8_t* blocks, const float* x, float* out, 
     const int64_t nb = K / F::kBK;
     const int64_t total = N * nb * F::kBB;
     const int64_t want = (N + kWarps - 1) / kWarps;
-    const int64_t cap = 4LL * num_sms();   // 4 CTAs of 8 warps per SM (up to 48 KB of stages each)
+    const size_t ring = (size_t)kWarps * F::kStages * F::kCPL * 512;
+    const bool xsm = K <= kMaxSmemX;
+    const size_t smem = ring + (xsm ? (size_t)K * 4 : 0);
+    // CTAs of 8 warps per SM: up to 4, as many as the shared memory holds
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(4, (int64_t)(227 * 1024) / (int64_t)(smem + 1024)));
+    const int64_t cap = per_sm * num_sms();
     const unsigned grid = (unsigned)(want < cap ? want : cap);
-    return launch_pdl(gguf_gemv_kernel<FMT>, dim3(grid), dim3(kWarps * 32), 0, s, blocks, x, out, N, nb, total);
+    if (!xsm) return launch_pdl(gguf_gemv_kernel<FMT, false>, dim3(grid), dim3(kWarps * 32), smem, s, blocks, x, out, N, nb, total);
+    static unsigned long long configured = 0ull;   // bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(configured & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(gguf_gemv_kernel<FMT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(ring + kMaxSmemX * 4));
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured |= 1ull << dev;
+    }
+    return launch_pdl(gguf_gemv_kernel<FMT, true>, dim3(grid), dim3(kWarps * 32), smem, s, blocks, x, out, N, nb, total);
 }
 
 }  // namespace
@@ -229,14 +279,14 @@ extern "C" {
 
 gai4_status gai4_q8_0_34b_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K,
                                void* stream) {
-    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 32 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 32 != 0 || K >= (1LL << 31)) return GAI4_ERR_INVALID_ARG;
     if (((uintptr_t)blocks & 15u) != 0 || ((uintptr_t)x & 15u) != 0) return GAI4_ERR_MISALIGNED;
     return gai4::launch_gguf_gemv<0>(blocks, x, out, N, K, (cudaStream_t)stream) == cudaSuccess ? GAI4_OK
                                                                                                 : GAI4_ERR_CUDA;
 }
 
 gai4_status gai4_q6_k_gemv(const uint8_t* blocks, const float* x, float* out, int64_t N, int64_t K, void* stream) {
-    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 256 != 0) return GAI4_ERR_INVALID_ARG;
+    if (!blocks || !x || !out || N <= 0 || K <= 0 || K % 256 != 0 || K >= (1LL << 31)) return GAI4_ERR_INVALID_ARG;
     if (((uintptr_t)blocks & 15u) != 0 || ((uintptr_t)x & 15u) != 0) return GAI4_ERR_MISALIGNED;
     return gai4::launch_gguf_gemv<1>(blocks, x, out, N, K, (cudaStream_t)stream) == cudaSuccess ? GAI4_OK
                                                                                                 : GAI4_ERR_CUDA;

@@ -299,8 +299,8 @@ gai4_status gai4_q4_k_dequantize(const uint8_t* blocks, float* w_out, int64_t N,
  * format's published block definitions):
  *   blocks [N, K/32, 34] bytes: bytes 0..1 the f16 scale d (little-endian),
  *   bytes 2..33 the 32 int8 codes; out[n] = sum_b d[n,b] * sum_j q[n,b,j] x[32b + j].
- *   x [K] float32, out [N] float32. K a multiple of 32; blocks and x 16-byte
- *   aligned (rows themselves need not be: a row is K/32 * 34 bytes).
+ *   x [K] float32, out [N] float32. K a multiple of 32 below 2^31; blocks and
+ *   x 16-byte aligned (rows themselves need not be: a row is K/32 * 34 bytes).
  */
 gai4_status gai4_q8_0_34b_gemv(const uint8_t* blocks, const float* x, float* out,
                                int64_t N, int64_t K, void* stream);
@@ -315,8 +315,8 @@ gai4_status gai4_q8_0_34b_gemv(const uint8_t* blocks, const float* x, float* out
  *     q = (nibble c/2 of ql[64h + 32(c%2) + l], low nibble first)
  *       + 16 * (bits 2c..2c+1 of qh[32h + l]) - 32          (-32 .. 31)
  *   and the weight d * sc[e/16] * q. out[n] = sum_k w[n,k] x[k];
- *   x [K] float32, out [N] float32. K a multiple of 256; blocks and x
- *   16-byte aligned.
+ *   x [K] float32, out [N] float32. K a multiple of 256 below 2^31; blocks
+ *   and x 16-byte aligned.
  */
 gai4_status gai4_q6_k_gemv(const uint8_t* blocks, const float* x, float* out,
                            int64_t N, int64_t K, void* stream);

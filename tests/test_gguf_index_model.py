@@ -23,8 +23,20 @@ def _consts():
         m = re.search(r"struct GgufFmt<%d> \{[^}]*?static constexpr int ([^;]*);" % fmt, text, re.S)
         out[fmt] = {k.strip(): int(v) for k, v in (kv.split("=") for kv in m.group(1).split(","))}
     out["warps"] = int(re.search(r"constexpr int kWarps = (\d+);", text).group(1))
-    out["ctas_per_sm"] = int(re.search(r"const int64_t cap = (\d+)LL \* num_sms\(\)", text).group(1))
+    m = re.search(r"std::min<int64_t>\((\d+), \(int64_t\)\((\d+) \* 1024\) / \(int64_t\)\(smem \+ (\d+)\)\)", text)
+    out["ctas_per_sm_max"], out["smem_kb"], out["smem_slack"] = (int(g) for g in m.groups())
+    out["max_smem_x"] = int(re.search(r"constexpr int64_t kMaxSmemX = (\d+);", text).group(1))
     return out
+
+
+def _grid(fmt, N, K, sms):
+    """The launcher's grid: CTAs of kWarps warps, as many per SM as the shared
+    memory (stage ring, plus x when it is staged) allows, up to the cap."""
+    F = C[fmt]
+    ring = C["warps"] * F["kStages"] * F["kCPL"] * 512
+    smem = ring + (4 * K if K <= C["max_smem_x"] else 0)
+    per_sm = max(1, min(C["ctas_per_sm_max"], (C["smem_kb"] * 1024) // (smem + C["smem_slack"])))
+    return min((N + C["warps"] - 1) // C["warps"], per_sm * sms), smem
 
 
 C = _consts()
@@ -47,7 +59,8 @@ def _model(fmt, N, K, sms=152, flat=None, x=None):
     RB = nb * BB
     nslab = (nb + SB - 1) // SB
     warps = C["warps"]
-    grid = min((N + warps - 1) // warps, C["ctas_per_sm"] * sms)
+    grid, smem = _grid(fmt, N, K, sms)
+    assert smem <= C["smem_kb"] * 1024
     wstride = grid * warps
     out = np.full(N, np.nan)
     written = np.zeros(N, dtype=np.int64)

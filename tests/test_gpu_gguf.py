@@ -31,14 +31,16 @@ def _run(fmt, N, K, seed, rows=None):
     assert_within(got, ref, absdot, "f32", f"{fmt} N={N} K={K}")
 
 
+# K up to 24576 stages x in shared memory; (3, 24576) is the largest such K,
+# (2, 32768) reads x through the read-only cache
 @pytest.mark.parametrize("N,K", [(1, 32), (3, 96), (7, 1024), (9, 1056), (129, 4096), (1000, 5120), (33, 14336),
-                                 (4099, 3072), (5, 32 * 33)])
+                                 (4099, 3072), (5, 32 * 33), (3, 24576), (2, 32768)])
 def test_q8_0_34b_gemv(N, K):
     _run("q8_0_34b", N, K, N + K)
 
 
 @pytest.mark.parametrize("N,K", [(1, 256), (3, 768), (7, 2048), (9, 2304), (129, 4096), (1000, 5120),
-                                 (33, 14336), (4099, 3072), (3, 256 * 17)])
+                                 (33, 14336), (4099, 3072), (3, 256 * 17), (3, 24576), (2, 32768)])
 def test_q6_k_gemv(N, K):
     _run("q6_k", N, K, 2 * N + K)
 
