@@ -23,9 +23,10 @@
 // zero-fills the rest); words at 2-byte-aligned offsets are then read from the
 // stage as two aligned words and a funnel shift.
 // A code c becomes a float through the mantissa of 2^23: a byte permute puts
-// c under the exponent byte 0x4B, and one subtraction removes 2^23 and the
-// code's offset (128 for Q8_0 bytes with the sign bit flipped, 32 for Q6_K)
-// exactly. Products and sums are binary32; the block scale is applied once
+// c under the exponent byte 0x4B, and one packed subtraction per pair of codes
+// (add.rn.f32x2) removes 2^23 and the codes' offset (128 for Q8_0 bytes with
+// the sign bit flipped, 32 for Q6_K) exactly; one fma.rn.f32x2 adds both
+// products. Products and sums are binary32; the block scale is applied once
 // per block (Q8_0) or once per 4-weight run of one 16-weight scale group
 // (Q6_K), and a warp-shuffle sum finishes each row.
 #include <stdint.h>
@@ -76,10 +77,30 @@ __device__ __forceinline__ uint32_t lds_u32_at(const uint8_t* buf, int o) {
     return __funnelshift_r(w[0], w[1], (o & 3) * 8);
 }
 
-// byte k of v as the float 2^23 + byte, minus `off`
+// byte k of v under the exponent of 2^23: the float 2^23 + byte (bits)
 template <int k>
-__device__ __forceinline__ float code_f(uint32_t v, float off) {
-    return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7650 | k)) - off;
+__device__ __forceinline__ uint32_t code_bits(uint32_t v) {
+    return __byte_perm(v, 0x4B000000u, 0x7650 | k);
+}
+// bytes k, k + 1 of v as the exact pair (byte - off'): one packed subtract of
+// (2^23 + off') from (2^23 + byte_k, 2^23 + byte_{k+1}); noff = -(2^23 + off')
+template <int k>
+__device__ __forceinline__ float2 code_pair(uint32_t v, float noff) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n add.rn.f32x2 d, a, b;\n"
+        " mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(code_bits<k>(v)), "r"(code_bits<k + 1>(v)), "f"(noff));
+    return d;
+}
+// (c.x + a.x b.x, c.y + a.y b.y) in one instruction (fma.rn.f32x2)
+__device__ __forceinline__ float2 ffma2(float2 a, float bx, float by, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(bx), "f"(by), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 // 16-byte asynchronous copy global -> shared that reads `src_bytes` (1..16)
@@ -104,19 +125,17 @@ __device__ __forceinline__ float decode_q8_0_34(const uint8_t* buf, int m, const
     const int b0 = slab * GgufFmt<0>::kSB;
     const int nbs = min(GgufFmt<0>::kSB, nb - b0);
     const int e4 = (lane & 7) * 4;
-    const float off = 8388736.0f;   // 2^23 + 128
+    const float noff = -8388736.0f;   // -(2^23 + 128)
     float acc = 0.f;
 #pragma unroll 2
     for (int jb = lane >> 3; jb < nbs; jb += 4) {
         const int o = m + 34 * jb;
         const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(buf + o));
-        const uint32_t w = lds_u32_at(buf, o + 2 + e4) ^ 0x80808080u;
+        const uint32_t w = lds_u32_at(buf, o + 2 + e4) ^ 0x80808080u;   // codes + 128, as bytes
         const float4 xv = ld_x4<XSM>(x + (b0 + jb) * 32 + e4);
-        float s = code_f<0>(w, off) * xv.x;
-        s = fmaf(code_f<1>(w, off), xv.y, s);
-        s = fmaf(code_f<2>(w, off), xv.z, s);
-        s = fmaf(code_f<3>(w, off), xv.w, s);
-        acc = fmaf(d, s, acc);
+        float2 s2 = ffma2(code_pair<0>(w, noff), xv.x, xv.y, make_float2(0.f, 0.f));
+        s2 = ffma2(code_pair<2>(w, noff), xv.z, xv.w, s2);
+        acc = fmaf(d, s2.x + s2.y, acc);
     }
     return acc;
 }
@@ -134,7 +153,7 @@ __device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const fl
     const int nbs = min(GgufFmt<1>::kSB, nb - b0);
     const int h = lane >> 4, r = (lane & 15) * 4;
     const int csh = (r >> 5) * 2;
-    const float off = 8388640.0f;   // 2^23 + 32
+    const float noff = -8388640.0f;   // -(2^23 + 32)
     float acc = 0.f;
 #pragma unroll 2
     for (int jb = 0; jb < nbs; ++jb) {
@@ -149,15 +168,11 @@ __device__ __forceinline__ float decode_q6_k(const uint8_t* buf, int m, const fl
         const float4 xh = ld_x4<XSM>(xb + 64);
         const uint32_t lo = (qlw & 0x0F0F0F0Fu) | ((q2 << 4) & 0x30303030u);
         const uint32_t hi = ((qlw >> 4) & 0x0F0F0F0Fu) | (q2 & 0x30303030u);
-        float a = code_f<0>(lo, off) * xl.x;
-        a = fmaf(code_f<1>(lo, off), xl.y, a);
-        a = fmaf(code_f<2>(lo, off), xl.z, a);
-        a = fmaf(code_f<3>(lo, off), xl.w, a);
-        float b = code_f<0>(hi, off) * xh.x;
-        b = fmaf(code_f<1>(hi, off), xh.y, b);
-        b = fmaf(code_f<2>(hi, off), xh.z, b);
-        b = fmaf(code_f<3>(hi, off), xh.w, b);
-        acc = fmaf(d, fmaf(sl, a, sh * b), acc);
+        float2 a2 = ffma2(code_pair<0>(lo, noff), xl.x, xl.y, make_float2(0.f, 0.f));
+        a2 = ffma2(code_pair<2>(lo, noff), xl.z, xl.w, a2);
+        float2 b2 = ffma2(code_pair<0>(hi, noff), xh.x, xh.y, make_float2(0.f, 0.f));
+        b2 = ffma2(code_pair<2>(hi, noff), xh.z, xh.w, b2);
+        acc = fmaf(d, fmaf(sl, a2.x + a2.y, sh * (b2.x + b2.y)), acc);
     }
     return acc;
 }
