@@ -96,9 +96,10 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(family):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if the summary was taken on the current kernel source."""
+def recorded_traffic(family, algorithmic_bytes):
+    """DRAM bytes per step of a family from the committed ncu summary, if the
+    summary was taken on the current kernel source and on this workload (the
+    same algorithmic bytes per step: a run restricted by --only is not)."""
     path = os.path.join(ROOT, "profiles", f"{family}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -110,6 +111,8 @@ def recorded_traffic(family):
     if vals.get("source_sha256_16") != source_hash(KERNEL_SOURCES[family]):
         return None
     try:
+        if int(vals["algorithmic_bytes_per_step"]) != int(algorithmic_bytes):
+            return None
         return float(vals["dram_bytes_per_step"])
     except (KeyError, ValueError):
         return None
@@ -579,7 +582,7 @@ def run_gpu(args, rank, world, local_rank):
     dom_ms = fam_ms[dom]
     n_launch = len(calls[dom])
     achieved = fam_bytes[dom] / (dom_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(dom)
+    traffic = recorded_traffic(dom, fam_bytes[dom])
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
